@@ -1,0 +1,246 @@
+"""FCFS continuous-batching scheduler oracle (test infrastructure only).
+
+An event simulator of the iteration-level scheduler that decides, step by step,
+which tokens of which requests run, and that owns the paged KV block pool.  It
+produces the per-step metadata of the attention step (request order, new tokens,
+stored tokens, block tables, slot mapping) and nothing else: no attention is
+computed here.
+
+Sources:
+* [KVN] §Continuous Batching原理: each iteration retires finished requests, admits
+  new ones and runs one step for every running request.
+* [KVN] §调度策略: first-come-first-served order; preemption when GPU memory
+  runs out.
+* [CB] §Chunked prefill / §Continuous batching: a prompt may be processed in
+  chunks; prefill and decode tokens share one ragged batch whose size is bounded
+  by a token budget m.
+* [SM] §PagedAttention 批处理: a new physical block is taken only once the
+  request's current block is full.
+
+Readings (the algorithm figure of [CB] §Continuous batching is missing; the
+pages leave these points open):
+1. Per request: P prompt tokens, O output tokens, g produced so far, c tokens
+   whose KV is stored.  The known tokens are the P prompt tokens followed by the
+   g produced ones; a step processes positions c .. c+n-1 of them, and when it
+   reaches the last known token (c + n == P + g) it produces one more token.
+   A request with exactly one position left to process is "decoding".  It is
+   finished when g == O, so it processes P + O - 1 positions in all.
+2. Each step, in this order:
+   a. arrivals (arrival step <= now) join the waiting queue in arrival order;
+   b. running decoding requests, in arrival order, get 1 token each; when one
+      needs a block and none is free, the latest-arrived running request that
+      has nothing scheduled in this step is preempted (this may be the request
+      itself);
+   c. running requests still prefilling, in arrival order, get
+      min(remaining, budget left) tokens; to find blocks they may preempt only
+      later-arrived running requests with nothing scheduled; the chunk is cut to
+      the tokens that fit;
+   d. waiting requests are admitted in queue order while budget is left; the
+      first chunk is min(remaining, budget left, tokens that fit in free blocks);
+      admission stops at the first request that gets no token or that was
+      preempted in this same step (no preemption, no skipping ahead).
+   Then every scheduled request advances, and finished ones return their blocks.
+3. Preemption is by recompute (swapping is not described): the victim returns
+   all its blocks, keeps its produced tokens and goes back to the waiting queue
+   with c = 0, so its next prefill covers P + g positions.  The waiting queue is
+   kept in arrival order (ties in arrival step broken by request id), so a
+   preempted request is served before every request that arrived after it.
+   "Latest-arrived" likewise means the largest request id.
+4. The free list is FIFO: blocks are taken from its front and returned to its
+   back in block-table order; its initial order is an input (a seeded
+   permutation of the pool, so blocks are scattered).
+5. A request needing more blocks than the whole pool can ever hold
+   (ceil((P + O - 1) / block_size) > num_blocks) is rejected on arrival.
+"""
+from collections import deque
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+@dataclass
+class Request:
+    rid: int
+    arrival: int
+    prompt_len: int
+    output_len: int
+    produced: int = 0          # g
+    stored: int = 0            # c
+    blocks: list = field(default_factory=list)
+    state: str = "pending"     # pending, waiting, running, finished, rejected
+    preemptions: int = 0
+
+    @property
+    def remaining(self):
+        return self.prompt_len + self.produced - self.stored
+
+
+@dataclass
+class StepMetadata:
+    step: int
+    req_ids: np.ndarray       # int32 [B], batch order
+    q_lens: np.ndarray        # int32 [B]
+    ctx_lens: np.ndarray      # int32 [B] tokens stored before this step
+    block_tables: list        # list of int lists: valid entries only
+    slot_mapping: np.ndarray  # int64 [sum(q_lens)]
+    preempted: list           # request ids preempted during this step
+    finished: list            # request ids that finished at the end of this step
+
+
+def _blocks_for(n_tokens, block_size):
+    return -(-n_tokens // block_size)
+
+
+class FCFSScheduler:
+    def __init__(self, requests, token_budget, block_size, num_blocks, free_order):
+        """requests: iterable of (arrival_step, prompt_len, output_len), ids = index,
+        sorted by arrival.  free_order: the initial free-list order (a permutation
+        of range(num_blocks))."""
+        self.reqs = [Request(i, int(a), int(p), int(o)) for i, (a, p, o) in enumerate(requests)]
+        arrivals = [r.arrival for r in self.reqs]
+        assert arrivals == sorted(arrivals), "requests must be given in arrival order"
+        assert sorted(int(b) for b in free_order) == list(range(num_blocks))
+        self.budget = int(token_budget)
+        self.bs = int(block_size)
+        self.num_blocks = int(num_blocks)
+        self.free = deque(int(b) for b in free_order)
+        self.pending = deque(self.reqs)
+        self.waiting = []          # kept in arrival (id) order, head first
+        self.running = []          # kept in arrival (id) order
+        self.now = 0
+
+    # --- allocator -------------------------------------------------------
+    def _grow(self, req, n_tokens):
+        need = _blocks_for(n_tokens, self.bs) - len(req.blocks)
+        for _ in range(need):
+            req.blocks.append(self.free.popleft())
+
+    def _release(self, req):
+        for b in req.blocks:
+            self.free.append(b)
+        req.blocks = []
+
+    def _preempt(self, req):
+        self._release(req)
+        req.stored = 0
+        req.state = "waiting"
+        req.preemptions += 1
+        self.running.remove(req)
+        self.waiting.append(req)
+        self.waiting.sort(key=lambda r: r.rid)
+
+    # --- one iteration ---------------------------------------------------
+    def done(self):
+        return not self.pending and not self.waiting and not self.running
+
+    def step(self):
+        while self.pending and self.pending[0].arrival <= self.now:
+            r = self.pending.popleft()
+            if _blocks_for(r.prompt_len + r.output_len - 1, self.bs) > self.num_blocks:
+                r.state = "rejected"
+                continue
+            r.state = "waiting"
+            self.waiting.append(r)
+
+        budget = self.budget
+        sched = []                 # (req, n_tokens, stored_before)
+        scheduled_ids = set()
+        preempted = []
+
+        def victim(after_rid):
+            cands = [r for r in self.running
+                     if r.rid not in scheduled_ids and r.rid > after_rid]
+            return max(cands, key=lambda r: r.rid) if cands else None
+
+        # b. running decodes
+        for req in list(self.running):
+            if budget == 0:
+                break
+            if req.state != "running" or req.remaining != 1:
+                continue
+            while _blocks_for(req.stored + 1, self.bs) - len(req.blocks) > len(self.free):
+                v = victim(req.rid - 1)              # candidates include req itself
+                self._preempt(v)
+                preempted.append(v.rid)
+                if v is req:
+                    break
+            if req.state != "running":
+                continue
+            self._grow(req, req.stored + 1)
+            sched.append((req, 1, req.stored))
+            scheduled_ids.add(req.rid)
+            budget -= 1
+
+        # c. running prefills
+        for req in list(self.running):
+            if budget == 0:
+                break
+            if req.state != "running" or req.rid in scheduled_ids or req.remaining <= 1:
+                continue
+            want = min(req.remaining, budget)
+            while _blocks_for(req.stored + want, self.bs) - len(req.blocks) > len(self.free):
+                v = victim(req.rid)
+                if v is None:
+                    break
+                self._preempt(v)
+                preempted.append(v.rid)
+            fit = (len(req.blocks) + len(self.free)) * self.bs - req.stored
+            n = min(want, fit)
+            if n <= 0:
+                continue
+            self._grow(req, req.stored + n)
+            sched.append((req, n, req.stored))
+            scheduled_ids.add(req.rid)
+            budget -= n
+
+        # d. admissions
+        while self.waiting and budget > 0:
+            req = self.waiting[0]
+            if req.rid in preempted:
+                break
+            n = min(req.remaining, budget, len(self.free) * self.bs)
+            if n <= 0:
+                break
+            self.waiting.pop(0)
+            req.state = "running"
+            self.running.append(req)
+            self.running.sort(key=lambda r: r.rid)
+            self._grow(req, req.stored + n)
+            sched.append((req, n, req.stored))
+            scheduled_ids.add(req.rid)
+            budget -= n
+
+        # metadata
+        slots = []
+        for req, n, c in sched:
+            for p in range(c, c + n):
+                slots.append(req.blocks[p // self.bs] * self.bs + p % self.bs)
+        meta = StepMetadata(
+            step=self.now,
+            req_ids=np.array([r.rid for r, _, _ in sched], dtype=np.int32),
+            q_lens=np.array([n for _, n, _ in sched], dtype=np.int32),
+            ctx_lens=np.array([c for _, _, c in sched], dtype=np.int32),
+            block_tables=[list(r.blocks) for r, _, _ in sched],
+            slot_mapping=np.array(slots, dtype=np.int64),
+            preempted=preempted,
+            finished=[],
+        )
+
+        # the forward pass happens here; then every scheduled request advances
+        for req, n, _ in sched:
+            req.stored += n
+            if req.stored == req.prompt_len + req.produced:
+                req.produced += 1
+            if req.produced == req.output_len:
+                req.state = "finished"
+                self._release(req)
+                self.running.remove(req)
+                meta.finished.append(req.rid)
+        self.now += 1
+        return meta
+
+    def run(self, max_steps=1_000_000):
+        out = []
+        while not self.done() and self.now < max_steps:
+            out.append(self.step())
+        return out

@@ -1,0 +1,136 @@
+"""Pins of the FCFS scheduler oracle: the pages' worked examples and invariants
+that any correct paged, chunked, preempting FCFS scheduler must keep."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import paged as op
+from oracle.scheduler import FCFSScheduler
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def test_chunked_prefill_worked_example(golden_dir):
+    """[CB] §Chunked prefill: a 7-token prompt with room for 4 tokens per pass runs
+    as a 4-token chunk and then a 3-token chunk after 4 stored tokens."""
+    g = _load(golden_dir, "chunking_n7_m4.json")
+    s = FCFSScheduler([(0, g["n"], 1)], token_budget=g["m"], block_size=16, num_blocks=4,
+                      free_order=range(4))
+    steps = s.run()
+    assert [m.q_lens.tolist() for m in steps] == [[q] for q in g["chunk_sizes"]]
+    assert [m.ctx_lens.tolist() for m in steps] == [[c] for c in g["chunk_ctx"]]
+    assert s.reqs[0].state == "finished" and s.reqs[0].produced == 1
+
+
+def test_iteration_level_example(golden_dir):
+    """[KVN] §Iteration-level调度详解: req3 finishes and req5 joins the next step."""
+    g = _load(golden_dir, "iteration_example.json")
+    reqs = [(0, 1, 50), (0, 1, 50), (0, 1, 2), (0, 1, 50), (2, 1, 50)]
+    s = FCFSScheduler(reqs, token_budget=64, block_size=16, num_blocks=64, free_order=range(64))
+    s.step()                        # step 0: the four prompts are prefilled
+    t = s.step()                    # step t: four decodes; req3 produces its last token
+    t1 = s.step()                   # step t+1
+    assert (t.req_ids + 1).tolist() == g["batch_t"]
+    assert t.finished == [2]
+    assert (t1.req_ids + 1).tolist() == g["batch_t_plus_1"]
+
+
+def test_decode_takes_a_block_only_when_the_last_is_full():
+    """[SM] §PagedAttention 批处理: a new block only once the current one is full."""
+    s = FCFSScheduler([(0, 15, 4)], token_budget=64, block_size=16, num_blocks=8, free_order=range(8))
+    m0 = s.step()                   # prefill 15 tokens -> 1 block
+    assert m0.block_tables == [[0]]
+    m1 = s.step()                   # decode position 15 -> still block 0
+    assert m1.block_tables == [[0]] and m1.slot_mapping.tolist() == [15]
+    m2 = s.step()                   # decode position 16 -> second block
+    assert m2.block_tables == [[0, 1]] and m2.slot_mapping.tolist() == [16]
+
+
+def test_preemption_by_recompute_small_case():
+    """Pool of 2 blocks (32 tokens): two 16-token prompts fill it; when the first
+    needs a third block the later request is preempted and later recomputed."""
+    s = FCFSScheduler([(0, 16, 3), (0, 16, 3)], token_budget=64, block_size=16,
+                      num_blocks=2, free_order=[1, 0])
+    m0 = s.step()
+    assert m0.q_lens.tolist() == [16, 16] and m0.block_tables == [[1], [0]]
+    m1 = s.step()                   # request 0 decodes position 16 -> needs a block
+    assert m1.preempted == [1]
+    assert m1.req_ids.tolist() == [0] and m1.block_tables == [[1, 0]]
+    steps = [m0, m1] + s.run()
+    r1 = s.reqs[1]
+    assert r1.state == "finished" and r1.preemptions == 1
+    # request 1 recomputes its prompt plus the one token it had produced (16 + 1)
+    rec = [m for m in steps if 1 in m.req_ids.tolist() and m.ctx_lens[m.req_ids.tolist().index(1)] == 0]
+    assert [int(m.q_lens[m.req_ids.tolist().index(1)]) for m in rec] == [16, 17]
+
+
+def _check_trace(tr, max_steps=100000):
+    s = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks,
+                      wl.free_order(tr.num_blocks, tr.seed))
+    steps = s.run(max_steps)
+    assert s.done(), "trace did not finish"
+    first_admit = []
+    last = {}
+    for m in steps:
+        ids = m.req_ids.tolist()
+        assert len(set(ids)) == len(ids)
+        assert int(m.q_lens.sum()) <= tr.token_budget
+        assert all(q >= 1 for q in m.q_lens.tolist())
+        seen = set()
+        for r, q, c, tab in zip(ids, m.q_lens.tolist(), m.ctx_lens.tolist(), m.block_tables):
+            assert len(tab) == -(-(c + q) // tr.block_size)
+            assert not (set(tab) & seen)
+            seen |= set(tab)
+            if r not in first_admit:
+                first_admit.append(r)
+            prev = last.get(r)
+            assert c == 0 or (prev is not None and c == prev), (r, c, prev)
+            last[r] = c + q
+        if m.preempted:
+            for r in m.preempted:
+                last[r] = 0
+        want = op.slot_mapping(m.block_tables, m.q_lens.tolist(), m.ctx_lens.tolist(), tr.block_size)
+        assert np.array_equal(m.slot_mapping, want)
+    assert first_admit == sorted(first_admit), "admission must follow arrival order"
+    for r in s.reqs:
+        if r.state == "rejected":
+            continue
+        assert r.state == "finished"
+        assert r.produced == r.output_len
+        assert r.stored == r.prompt_len + r.output_len - 1
+        assert r.blocks == []
+    assert sorted(s.free) == list(range(tr.num_blocks))
+    return s, steps
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_invariants_on_tight_small_traces(seed):
+    tr = wl.small_trace(seed)
+    s, steps = _check_trace(tr)
+    if seed < 4:
+        assert s.now > 0
+
+
+def test_tight_traces_do_preempt():
+    total = 0
+    for seed in range(12):
+        s, _ = _check_trace(wl.small_trace(seed))
+        total += sum(r.preemptions for r in s.reqs)
+    assert total > 0
+
+
+def test_block_ownership_is_exclusive_every_step():
+    tr = wl.small_trace(3, n_requests=30, num_blocks=24)
+    s = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks,
+                      wl.free_order(tr.num_blocks, tr.seed))
+    while not s.done():
+        s.step()
+        owned = [b for r in s.reqs for b in r.blocks]
+        assert len(owned) == len(set(owned))
+        assert sorted(owned + list(s.free)) == list(range(tr.num_blocks))
