@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of one continuous-batching attention step over a paged KV cache.
+
+A step = the whole hot path over one batch: the host slot mapping (e2e leg),
+the slot-mapped KV append and the paged attention launch (decode split-K,
+tensor-core prefill tiles, or both in one launch).  Default workload: 64 decode
+requests of a Llama-2-7B attention layer (MHA 32 x 128, contexts uniform in
+[512, 4096], block 16, 20 GB pool) -- about 2.4 GB of K/V read per step, far
+larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead, on bounded samples of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|mixed|mixed_budget|long|tiny]
+"""
+import os
+
+# the oracle (cpu baseline / reference arm) runs single-threaded, so "cores" is exact
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import workloads as wl  # noqa: E402
+
+METRIC = "mixed-step attention tokens/s; decode KV GB/s as % of measured HBM peak"
+UNIT = "tokens/s"
+WORKLOADS = {
+    "decode": (lambda seed: wl.decode(seed=seed),
+               "decode: 64 requests, ctx U[512,4096], MHA 32x128 (Llama-2-7B layer), bf16, block 16, 20 GB pool"),
+    "mixed": (lambda seed: wl.mixed(seed=seed),
+              "mixed: 48 decodes ctx U[256,8192] + 2x512-token chunks after 1024/3072, GQA 32/8 x128, bf16"),
+    "mixed_budget": (lambda seed: wl.mixed(seed=seed, budget_variant=True),
+                     "mixed, 560-token budget: 48 decodes + one 512-token chunk after 1024, GQA 32/8 x128"),
+    "long": (lambda seed: wl.long(15, seed=seed),
+             "long: 2048-token chunk after 30720 stored (step 15 of a 32768 prompt) + 16 decodes at 8207, GQA 32/8"),
+    "tiny": (lambda seed: wl.tiny(seed=seed), "tiny: 4 requests (37,1),(100,1),(4,3),(0,20), MHA 4x64"),
+}
+KERNEL_SOURCES = ["cb_common.cuh", "cb_decode_item.cuh", "cb_decode.cu", "cb_mixed.cu", "cb_api.cu"]
+
+
+# ---------------------------------------------------------------- work accounting
+def algorithmic(shape):
+    """Algorithmic work of one step: K/V bytes every request must read once
+    (valid tokens only), the new-token q/out/append bytes, and the causal-valid
+    attention FLOPs (QK^T and PV: 4 * A flops per (query head, key) pair)."""
+    a, hq, hk = shape.head_dim, shape.n_q_heads, shape.n_kv_heads
+    kv_bytes = dec_kv_bytes = 0
+    flops = pre_flops = 0
+    for c, n in zip(shape.ctx_lens, shape.q_lens):
+        if n == 0:
+            continue
+        kv_bytes += 2 * (c + n) * hk * a * 2
+        pairs = n * c + n * (n + 1) // 2
+        flops += 4 * a * hq * pairs
+        if n == 1:
+            dec_kv_bytes += 2 * (c + 1) * hk * a * 2
+        else:
+            pre_flops += 4 * a * hq * pairs
+    qo_bytes = 2 * shape.n_tokens * hq * a * 2
+    append_bytes = 2 * 2 * shape.n_tokens * hk * a * 2        # K and V rows, read + written
+    return dict(kv_bytes=kv_bytes, dec_kv_bytes=dec_kv_bytes, attn_bytes=kv_bytes + qo_bytes, flops=flops,
+                pre_flops=pre_flops, append_bytes=append_bytes)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_cb_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"cb_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_on_requests(shape, reqs, fetch):
+    """Run the fp64 oracle on whole requests `reqs`; `fetch(r)` returns that
+    request's (compact pool k, v, table, q rows, k_new rows, v_new rows) in fp64.
+    Returns (seconds, tokens)."""
+    from oracle import attention as oa
+    from oracle import paged as op
+    scale = 1.0 / math.sqrt(shape.head_dim)
+    data = [fetch(r) for r in reqs]
+    t0 = time.perf_counter()
+    toks = 0
+    for r, (kp, vp, table, q, kn, vn) in zip(reqs, data):
+        c, n = shape.ctx_lens[r], shape.q_lens[r]
+        k = np.concatenate([op.gather_request(kp, table, c, shape.block_size), kn])
+        v = np.concatenate([op.gather_request(vp, table, c, shape.block_size), vn])
+        oa.attention_step(q, [n], [c], [k], [v], scale, shape.n_q_heads, shape.n_kv_heads)
+        toks += n
+    return time.perf_counter() - t0, toks
+
+
+def cpu_fetch(shape, seed):
+    """Synthetic fp64 inputs of one request generated on the host (for the
+    reference arm, which needs no GPU): random blocks in a compact pool,
+    scattered by a seeded permutation."""
+    def fetch(r):
+        rng = np.random.default_rng(seed * 100003 + r)
+        c, n = shape.ctx_lens[r], shape.q_lens[r]
+        nblk = max(1, -(-c // shape.block_size))
+        pool = (nblk, shape.n_kv_heads, shape.block_size, shape.head_dim)
+        bf = lambda s: rng.standard_normal(size=s, dtype=np.float32).astype(np.float64)
+        kp, vp = bf(pool), bf(pool)
+        table = rng.permutation(nblk)
+        q = bf((n, shape.n_q_heads, shape.head_dim))
+        kn, vn = bf((n, shape.n_kv_heads, shape.head_dim)), bf((n, shape.n_kv_heads, shape.head_dim))
+        return kp, vp, table, q, kn, vn
+    return fetch
+
+
+def sample_requests(shape, budget_s, fetch, max_tokens=None):
+    """Grow a request sample (decodes first, in order) until ~budget_s of oracle time."""
+    order = [r for r in range(shape.n_reqs) if shape.q_lens[r] == 1] + \
+            [r for r in range(shape.n_reqs) if shape.q_lens[r] > 1 and shape.q_lens[r] <= 64]
+    if not order:
+        order = [int(np.argmin([q if q > 0 else 1 << 30 for q in shape.q_lens]))]
+    dt, toks = oracle_on_requests(shape, order[:1], fetch)
+    per = max(dt, 1e-4)
+    n = max(1, min(len(order), int(budget_s / per)))
+    if max_tokens:
+        n = min(n, max_tokens)
+    return order[:n]
+
+
+def run_reference(args, shape, desc, world, rank):
+    if rank != 0:
+        return
+    fetch = cpu_fetch(shape, shape.seed)
+    per_step = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    reqs = sample_requests(shape, per_step, fetch)
+    for _ in range(args.warmup):
+        oracle_on_requests(shape, reqs[:1], fetch)
+    total_t = total_tok = 0.0
+    for _ in range(args.steps):
+        dt, toks = oracle_on_requests(shape, reqs, fetch)
+        total_t += dt
+        total_tok += toks
+    value = total_tok / total_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "sample": f"{len(reqs)} request(s) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(reqs)} of {shape.n_reqs} requests per step, inputs generated on the host"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, shape, desc, world, rank, local):
+    import torch
+    from paged_kv_cache_cb_gb300 import _lib as L
+    if not os.path.exists(L.LIB_PATH):
+        from paged_kv_cache_cb_gb300 import build
+        build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    inp = wl.step_inputs_device(shape, dev)
+    bt_np = inp["block_tables"]
+    kv = [c + n for c, n in zip(shape.ctx_lens, shape.q_lens)]
+    max_q, max_kv = max(shape.q_lens), max(kv)
+    scale = 1.0 / math.sqrt(shape.head_dim)
+    slots_np = L.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, bt_np, shape.block_size)
+    cu_np = np.concatenate([[0], np.cumsum(shape.q_lens)]).astype(np.int32)
+    ctx_np = np.asarray(shape.ctx_lens, np.int32)
+    d_slots = torch.from_numpy(slots_np).to(dev)
+    d_cu = torch.from_numpy(cu_np).to(dev)
+    d_ctx = torch.from_numpy(ctx_np).to(dev)
+    d_bt = torch.from_numpy(bt_np).to(dev)
+    wsb = L.cb_paged_attention_workspace_size(shape.n_reqs, shape.n_tokens, max_q, max_kv, shape.n_q_heads,
+                                              shape.n_kv_heads, shape.head_dim, shape.block_size)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(inp["q"])
+    kc, vc = inp["k_pool"], inp["v_pool"]
+    launches = [0]
+
+    def step(q, k_new, v_new, slots, cu, ctx, bt, o):
+        L.cb_kv_append(k_new, v_new, slots, kc, vc, stream)
+        launches[0] += L.cb_last_launch_count()
+        L.cb_paged_attention(q, cu, ctx, bt, kc, vc, o, scale, ws, max_q, max_kv, stream)
+        launches[0] += L.cb_last_launch_count()
+
+    args_dev = (inp["q"], inp["k_new"], inp["v_new"], d_slots, d_cu, d_ctx, d_bt, out)
+    for _ in range(max(3, args.warmup)):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    status = L.cb_last_error(stream)
+    if status != 0:
+        raise RuntimeError("warm-up step failed: " + L.cb_strerror(status))
+
+    # HBM copy probe in the same process (context for the measured peak)
+    copy_gbs = None
+    if rank == 0:
+        nb = 4 << 30
+        a_ = torch.empty(nb, dtype=torch.uint8, device=dev)
+        b_ = torch.empty(nb, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            L.cb_hbm_copy(b_, a_, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            L.cb_hbm_copy(b_, a_, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        copy_gbs = 2 * nb * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del a_, b_
+
+    # ---- device-resident timed region
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    launches[0] = 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        L.cb_kv_append(inp["k_new"], inp["v_new"], d_slots, kc, vc, stream)
+        launches[0] += L.cb_last_launch_count()
+        ev[i][0].record(stream)
+        L.cb_paged_attention(inp["q"], d_cu, d_ctx, d_bt, kc, vc, out, scale, ws, max_q, max_kv, stream)
+        ev[i][1].record(stream)
+        launches[0] += L.cb_last_launch_count()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    status = L.cb_last_error(stream)
+    if status != 0:
+        raise RuntimeError("timed steps failed: " + L.cb_strerror(status))
+    elapsed = t_start.elapsed_time(t_end) * 1e-3
+    attn_s = sum(a.elapsed_time(b) for a, b in ev) * 1e-3 / args.steps
+    elapsed = max_over_ranks(elapsed, world, dev)
+    gpu_launches = launches[0]
+
+    # ---- end to end through the C ABI with host buffers
+    e2e_steps = max(3, min(args.steps, 200))
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_k, h_v = pin(inp["q"]), pin(inp["k_new"]), pin(inp["v_new"])
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_cu = torch.from_numpy(cu_np).pin_memory()
+    h_ctx = torch.from_numpy(ctx_np).pin_memory()
+    h_bt = torch.from_numpy(bt_np).pin_memory()
+    h_slots = torch.empty(shape.n_tokens, dtype=torch.int64).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(inp["q"]), torch.empty_like(inp["k_new"]), torch.empty_like(inp["v_new"])
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cu, h_ctx, h_bt, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        h_slots.numpy()[:] = L.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, bt_np, shape.block_size)
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        d_ctx.copy_(h_ctx, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        step(d_q, d_k, d_v, d_slots, d_cu, d_ctx, d_bt, out)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+
+    # ---- cpu baseline: the oracle on a bounded sample of this same step
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cu = cu_np
+
+        def fetch(r):
+            c = shape.ctx_lens[r]
+            nblk = -(-c // shape.block_size)
+            idx = torch.from_numpy(bt_np[r, :nblk].astype(np.int64)).to(dev)
+            f = lambda t: t.to("cpu", torch.float64).numpy()
+            return (f(kc.index_select(0, idx)), f(vc.index_select(0, idx)), np.arange(nblk),
+                    f(inp["q"][cu[r]:cu[r + 1]]), f(inp["k_new"][cu[r]:cu[r + 1]]), f(inp["v_new"][cu[r]:cu[r + 1]]))
+        reqs = sample_requests(shape, 12.0, fetch)
+        dt, toks = oracle_on_requests(shape, reqs, fetch)
+        cpu = {"value": toks / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{len(reqs)} of {shape.n_reqs} requests of the same step ({toks} tokens), fp64 NumPy, "
+                         f"{dt:.1f} s"}
+
+    if rank != 0:
+        return
+    work = algorithmic(shape)
+    peaks = load_peaks()
+    t_hbm = work["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = work["attn_bytes"] / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
+                "kernel": "paged attention launch (split-K decode / mixed)",
+                "algorithmic_bytes_per_launch": work["attn_bytes"], "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        achieved = work["flops"] / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": ncu_traffic(args.workload),
+                "kernel": "paged attention launch (tcgen05 prefill tiles + decode)",
+                "algorithmic_flops_per_launch": work["flops"], "peak_source": peaks["source"] + " bf16_tflops"}
+    value = shape.n_tokens * args.steps * world / elapsed
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": desc, "n_reqs": shape.n_reqs, "n_tokens": shape.n_tokens,
+                   "n_q_heads": shape.n_q_heads, "n_kv_heads": shape.n_kv_heads, "head_dim": shape.head_dim,
+                   "block_size": shape.block_size, "num_blocks": shape.num_blocks,
+                   "l2": f"inputs larger than L2: {work['kv_bytes'] / 1e9:.2f} GB K/V read per step, no flush",
+                   "parallelism": f"replicas x{world} (requests independent, no collective)"},
+        "roofline": roof,
+        "kv_gbs": work["kv_bytes"] / attn_s / 1e9,
+        "kv_frac_of_hbm_peak": work["kv_bytes"] / attn_s / 1e9 / peaks["hbm_gbs"],
+        "attention_ms": attn_s * 1e3,
+        "prefill_tflops": work["pre_flops"] / attn_s / 1e12 if work["pre_flops"] else None,
+        "copy_gbs_same_run": copy_gbs,
+        "cpu_baseline": cpu,
+        "e2e": {"value": shape.n_tokens * e2e_steps * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_env()
+    make, desc = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, make(args.seed), desc, world, rank)
+        return
+    # weak scaling: each rank runs its own batch of the same workload (its own seed)
+    run_ours(args, make(args.seed + rank), desc, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

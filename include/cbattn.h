@@ -1,0 +1,204 @@
+/*
+ * cbattn -- one continuous-batching attention step over a paged KV cache,
+ * for NVIDIA GB300 (sm_103a).  Plain C ABI: pointers and sizes only.
+ *
+ * Sources (pages on KV caching and continuous batching):
+ *  [CB]  "Continuous batching from first principles" (Chinese translation,
+ *        news.myit.tw): sections Attention, KV cache, Chunked prefill,
+ *        Continuous batching.
+ *  [SM]  "AWS SageMaker 推理方案" (clvsit.github.io): section PagedAttention 批处理.
+ *  [KVN] "KV Cache与Continuous Batching" notes (huajishe.fun): sections
+ *        MQA/GQA, Continuous Batching原理, 调度策略.
+ *  [KVB] "kv_cache" blog (klklkl10086.github.io): sections Batch Decode, 思想.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Element type of q, k_new, v_new, caches and out is bf16 (IEEE bfloat16,
+ *    passed as void*).  Accumulation is fp32.
+ *  - "device" pointers must point to memory of the current CUDA device; "host"
+ *    pointers to ordinary (or pinned) host memory.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every GPU entry
+ *    point only enqueues work and returns; nothing here synchronises except
+ *    cb_last_error().
+ *  - The caller owns every buffer.  Nothing allocates device memory per call.
+ *  - KV cache layout (both K and V): [num_blocks][n_kv_heads][block_size][head_dim],
+ *    row-major, so one (block, kv head) is block_size*head_dim contiguous values.
+ *    Token position p of a request lives in physical block
+ *    block_tables[r][p / block_size] at offset p % block_size ([SM] PagedAttention:
+ *    logical blocks mapped to physical blocks by a block table).
+ *  - Ragged batch ([CB] Continuous batching): requests are concatenated with no
+ *    batch dimension; request r owns query rows cu_q_lens[r] .. cu_q_lens[r+1]-1.
+ *    q and out are [n_tokens][n_q_heads][head_dim]; k_new and v_new are
+ *    [n_tokens][n_kv_heads][head_dim].
+ *  - GQA / MQA ([KVN] MQA/GQA): n_q_heads % n_kv_heads == 0 and query head h
+ *    reads KV head h / (n_q_heads / n_kv_heads).
+ *  - Supported shapes: head_dim 64 or 128; block_size 16;
+ *    n_q_heads / n_kv_heads in {1, 2, 4, 8}; n_reqs <= CB_MAX_REQS.
+ *  - Return value: CB_OK (0) on success, a negative CB_E* code otherwise.  Size
+ *    and pointer checks happen on the host before anything is enqueued; a
+ *    rejected call enqueues nothing.
+ */
+#ifndef CBATTN_H
+#define CBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CB_OK 0
+#define CB_EINVAL (-1)     /* bad size, unsupported shape, null pointer, misaligned pointer */
+#define CB_ECUDA (-2)      /* a CUDA runtime/driver call or kernel launch failed */
+#define CB_EWORKSPACE (-3) /* workspace too small (see cb_paged_attention_workspace_size) */
+#define CB_EDEVICE (-4)    /* a kernel found bad metadata (block id or slot out of range) */
+#define CB_ETIMEOUT (-5)   /* a kernel's bounded wait ran out; its outputs are undefined */
+#define CB_ESTATE (-6)     /* scheduler: bad request id / state, or capacity exceeded */
+
+#define CB_MAX_REQS 2048
+
+/* ---------------------------------------------------------------- KV append
+ * [CB] Chunked prefill ("store the KV states") and [SM] PagedAttention (new
+ * tokens' KV written into the request's physical blocks): for every new token
+ * t with slot_mapping[t] >= 0, for every KV head g,
+ *     k_cache[slot / block_size][g][slot % block_size][:] = k_new[t][g][:]
+ * and the same for v.  A negative slot skips the token.  The copy is bit-exact.
+ *
+ *  k_new, v_new   device, bf16 [n_tokens][n_kv_heads][head_dim]
+ *  slot_mapping   device, int64 [n_tokens]
+ *  k_cache,v_cache device, bf16 [num_blocks][n_kv_heads][block_size][head_dim]
+ * Errors: CB_EINVAL (sizes, null pointers, pointers not 16-byte aligned),
+ * CB_ECUDA (launch).  A slot >= num_blocks*block_size is not written; it sets
+ * the device error word (cb_last_error then returns CB_EDEVICE).
+ * Ordering: run it before cb_paged_attention of the same step on the same
+ * stream, so that attention sees the new keys.
+ */
+int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n_tokens,
+                 void* k_cache, void* v_cache, int num_blocks, int n_kv_heads, int head_dim,
+                 int block_size, void* stream);
+
+/* ---------------------------------------------------------------- attention
+ * One attention step ([CB] Attention, Chunked prefill, Continuous batching):
+ * for request r with ctx = ctx_lens[r] stored tokens and q_len new tokens, new
+ * token i (absolute position ctx + i) of query head h attends to keys
+ * 0 .. ctx + i of KV head g = h / (n_q_heads / n_kv_heads), read through
+ * block_tables[r]:
+ *     out[t][h] = softmax_j(scale * q[t][h] . K[j]) . V[j],   j <= ctx + i.
+ * The new tokens' keys must already be in the cache (cb_kv_append).  Requests
+ * never see each other's keys (the block-diagonal ragged mask).
+ * Decode requests (q_len == 1) run on CUDA cores, split over KV blocks, with the
+ * splits merged by log-sum-exp; requests with q_len > 1 run as 128-row tiles on
+ * the tensor cores.  Everything is one kernel launch (plus a memset of the
+ * workspace's counters).
+ *
+ *  q              device, bf16 [n_tokens][n_q_heads][head_dim]
+ *  cu_q_lens      device, int32 [n_reqs + 1], cu_q_lens[0] = 0, non-decreasing,
+ *                 cu_q_lens[n_reqs] = n_tokens
+ *  ctx_lens       device, int32 [n_reqs], >= 0
+ *  block_tables   device, int32 [n_reqs][max_blocks_per_seq]; entries past
+ *                 ceil((ctx + q_len) / block_size) are never read
+ *  max_q_len      host int, >= every q_len (1 selects the decode-only kernel)
+ *  max_kv_len     host int, >= every ctx + q_len; sizes the split-K workspace
+ *  k_cache,v_cache device, bf16 cache layout above
+ *  out            device, bf16 [n_tokens][n_q_heads][head_dim]
+ *  scale          multiplies q.k before the softmax (1/sqrt(head_dim) in the
+ *                 [KVB] Batch Decode listing)
+ *  workspace      device, >= cb_paged_attention_workspace_size(...) bytes,
+ *                 16-byte aligned; contents need no initialisation
+ * Errors: CB_EINVAL, CB_EWORKSPACE, CB_ECUDA.  Device-side metadata checks
+ * (block ids >= num_blocks, lengths beyond the table) skip the bad access and
+ * set the error word (cb_last_error -> CB_EDEVICE).
+ */
+int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                       const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                       int max_q_len, int max_kv_len, const void* k_cache, const void* v_cache,
+                       int num_blocks, void* out, float scale, int n_q_heads, int n_kv_heads,
+                       int head_dim, int block_size, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Bytes of workspace cb_paged_attention needs for these sizes (0 on invalid
+ * sizes).  Pure host function. */
+size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
+                                         int n_q_heads, int n_kv_heads, int head_dim, int block_size);
+
+/* Synchronise `stream`, then read and clear the device error word.
+ * Returns CB_OK, CB_EDEVICE, CB_ETIMEOUT or CB_ECUDA. */
+int cb_last_error(void* stream);
+
+/* Static description of an error code (never NULL). */
+const char* cb_strerror(int code);
+
+/* ---------------------------------------------------------------- measurement
+ * Device-to-device copy of `bytes` (multiple of 16, both pointers 16-byte
+ * aligned) with a plain streaming kernel: the HBM copy roofline probe. */
+int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/* Number of kernels the last successful cb_paged_attention / cb_kv_append call
+ * enqueued (for launch accounting in benchmarks). */
+int cb_last_launch_count(void);
+
+/* ---------------------------------------------------------------- host metadata
+ * Slot mapping of a step, on the host ([SM] PagedAttention: block table lookup):
+ * for request r and new token i, slot = table[r][(ctx+i) / bs] * bs + (ctx+i) % bs.
+ *  q_lens, ctx_lens  host int32 [n_reqs]; block_tables host int32
+ *  [n_reqs][max_blocks_per_seq]; slot_mapping_out host int64 [sum q_lens].
+ * Returns CB_OK or CB_EINVAL (a needed table entry is negative or the table is
+ * too short). */
+int cb_build_slot_mapping(const int32_t* q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
+                          int max_blocks_per_seq, int n_reqs, int block_size, int64_t* slot_mapping_out);
+
+/* ---------------------------------------------------------------- scheduler
+ * FCFS iteration-level continuous-batching scheduler with a paged block
+ * allocator and recompute preemption ([KVN] Continuous Batching原理 and 调度策略;
+ * [CB] Chunked prefill; [SM] PagedAttention: a block is taken only when the
+ * request's last block is full).  Host only; it produces the metadata of each
+ * step and never touches the GPU.  Rules, per step:
+ *   arrivals join the waiting queue; running decodes (one position left) get 1
+ *   token each in arrival order, preempting the latest-arrived unscheduled
+ *   running request when no block is free; running prefills get
+ *   min(remaining, budget left) tokens, preempting only later-arrived
+ *   unscheduled requests and otherwise cutting the chunk to what fits; waiting
+ *   requests are admitted in arrival order while budget remains, stopping at the
+ *   first that gets no token or was preempted in this step.  A preempted request
+ *   frees all blocks, keeps its produced tokens and later recomputes them.
+ *   The free list is FIFO, seeded by `free_order`.
+ * The opaque handle is owned by the caller and freed by cb_sched_destroy.
+ */
+typedef struct cb_sched cb_sched;
+
+/* free_order: host int32 [num_blocks], a permutation of 0..num_blocks-1 (the
+ * initial free-list order).  max_batch: capacity of one step's batch (requests). */
+cb_sched* cb_sched_create(int num_blocks, int block_size, int token_budget, int max_batch,
+                          const int32_t* free_order);
+void cb_sched_destroy(cb_sched* s);
+
+/* Register a request (ids are assigned 0, 1, 2, ... in call order; calls must
+ * come in non-decreasing arrival_step order).  Returns the id or CB_EINVAL. */
+int cb_sched_add_request(cb_sched* s, int arrival_step, int prompt_len, int output_len);
+
+/* Run one scheduling step and write its metadata into caller-owned host arrays:
+ *  req_ids [max_batch], q_lens [max_batch], ctx_lens [max_batch],
+ *  cu_q_lens [max_batch + 1], block_tables [max_batch][max_blocks_per_seq]
+ *  (unused entries -1), slot_mapping [token_budget] int64.
+ * *n_reqs_out / *n_tokens_out receive the batch size and token count.  Then
+ * advances every scheduled request as if the forward pass had run.  Returns the
+ * number of requests preempted in this step (>= 0), or CB_ESTATE when the batch
+ * does not fit the arrays. */
+int cb_sched_step(cb_sched* s, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
+                  int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
+                  int* n_tokens_out);
+
+/* 1 when no request is pending, waiting or running. */
+int cb_sched_done(const cb_sched* s);
+/* Free blocks right now. */
+int cb_sched_free_blocks(const cb_sched* s);
+/* Per-request state: produced tokens, stored tokens, preemption count, and
+ * state (0 pending, 1 waiting, 2 running, 3 finished, 4 rejected). */
+int cb_sched_request_info(const cb_sched* s, int req_id, int* produced, int* stored, int* preemptions,
+                          int* state);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CBATTN_H */

@@ -51,6 +51,9 @@ pages leave these points open):
    permutation of the pool, so blocks are scattered).
 5. A request needing more blocks than the whole pool can ever hold
    (ceil((P + O - 1) / block_size) > num_blocks) is rejected on arrival.
+6. Optional ``max_batch`` caps the number of requests in one step (each pass
+   stops once the batch holds that many); by default only the token budget
+   bounds the batch.
 """
 from collections import deque
 from dataclasses import dataclass, field
@@ -92,7 +95,7 @@ def _blocks_for(n_tokens, block_size):
 
 
 class FCFSScheduler:
-    def __init__(self, requests, token_budget, block_size, num_blocks, free_order):
+    def __init__(self, requests, token_budget, block_size, num_blocks, free_order, max_batch=None):
         """requests: iterable of (arrival_step, prompt_len, output_len), ids = index,
         sorted by arrival.  free_order: the initial free-list order (a permutation
         of range(num_blocks))."""
@@ -101,6 +104,7 @@ class FCFSScheduler:
         assert arrivals == sorted(arrivals), "requests must be given in arrival order"
         assert sorted(int(b) for b in free_order) == list(range(num_blocks))
         self.budget = int(token_budget)
+        self.max_batch = int(max_batch) if max_batch is not None else None
         self.bs = int(block_size)
         self.num_blocks = int(num_blocks)
         self.free = deque(int(b) for b in free_order)
@@ -147,6 +151,9 @@ class FCFSScheduler:
         scheduled_ids = set()
         preempted = []
 
+        def full():
+            return self.max_batch is not None and len(sched) >= self.max_batch
+
         def victim(after_rid):
             cands = [r for r in self.running
                      if r.rid not in scheduled_ids and r.rid > after_rid]
@@ -154,7 +161,7 @@ class FCFSScheduler:
 
         # b. running decodes
         for req in list(self.running):
-            if budget == 0:
+            if budget == 0 or full():
                 break
             if req.state != "running" or req.remaining != 1:
                 continue
@@ -173,7 +180,7 @@ class FCFSScheduler:
 
         # c. running prefills
         for req in list(self.running):
-            if budget == 0:
+            if budget == 0 or full():
                 break
             if req.state != "running" or req.rid in scheduled_ids or req.remaining <= 1:
                 continue
@@ -194,7 +201,7 @@ class FCFSScheduler:
             budget -= n
 
         # d. admissions
-        while self.waiting and budget > 0:
+        while self.waiting and budget > 0 and not full():
             req = self.waiting[0]
             if req.rid in preempted:
                 break

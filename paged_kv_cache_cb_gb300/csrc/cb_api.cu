@@ -1,0 +1,271 @@
+// C-ABI entry points of include/cbattn.h: argument checks, workspace carving,
+// TMA tensor-map encoding and kernel dispatch.  Host code only (plus the device
+// error word).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/cbattn.h"
+#include "cb_internal.h"
+
+namespace cb {
+
+__device__ unsigned int g_dev_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_last_launches = 0;
+
+struct DeviceInfo {
+  int n_sms = 0;
+  unsigned int* err = nullptr;
+};
+
+bool device_info(DeviceInfo* out) {
+  static DeviceInfo cache[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = cache[dev];
+  if (d.n_sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return false;
+    d.err = static_cast<unsigned int*>(p);
+    d.n_sms = sms;
+  }
+  *out = d;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Cache viewed as rows of head_dim values: [num_blocks * Hkv * block_size][A];
+// box = one (block, head) half-row group: 16 rows x 64 columns, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* cache, int num_blocks, int n_kv_heads, int head_dim) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * n_kv_heads * kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q viewed as [n_tokens][Hq][A]; box = 128/G tokens x the G heads of one group
+// x 64 columns, so one box is a 128-row query tile (row = token * G + head).
+bool encode_q_map(CUtensorMap* m, const void* q, int n_tokens, int n_q_heads, int head_dim, int group) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_q_heads, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_q_heads * head_dim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileM / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+// Smallest decode split the launcher may choose; the workspace is sized for it.
+constexpr int kMinSplitBlocks = 8;
+
+WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int split_blocks) {
+  WorkspaceLayout L{};
+  const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
+  const long long splits = (long long)n_reqs * ((nblk + split_blocks - 1) / split_blocks);
+  L.max_splits_total = (int)splits;
+  size_t off = 0;
+  L.counters = off;
+  off = align_up(off + (size_t)n_reqs * n_kv_heads * 4, 16);
+  L.queue = off;
+  off = align_up(off + 16, 256);
+  L.part_ml = off;
+  off = align_up(off + (size_t)splits * n_q_heads * 2 * 4, 256);
+  L.part_acc = off;
+  off = align_up(off + (size_t)splits * n_q_heads * head_dim * 4, 256);
+  L.total = off;
+  return L;
+}
+
+int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms) {
+  const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
+  const long long want = 4LL * n_sms * 8;           // items per decode warp slot, a few each
+  for (int sb = kMaxSplitBlocks; sb > kMinSplitBlocks; sb >>= 1)
+    if ((long long)n_reqs * n_kv_heads * ((nblk + sb - 1) / sb) >= want) return sb;
+  return kMinSplitBlocks;
+}
+
+}  // namespace cb
+
+using namespace cb;
+
+namespace {
+
+bool shape_ok(int n_q_heads, int n_kv_heads, int head_dim, int block_size) {
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return false;
+  const int g = n_q_heads / n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return false;
+  if (head_dim != 64 && head_dim != 128) return false;
+  return block_size == kBlockSize;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n_tokens, void* k_cache,
+                 void* v_cache, int num_blocks, int n_kv_heads, int head_dim, int block_size, void* stream) {
+  if (n_tokens < 0 || num_blocks <= 0 || n_kv_heads <= 0 || (head_dim != 64 && head_dim != 128) ||
+      block_size != kBlockSize)
+    return CB_EINVAL;
+  if (n_tokens == 0) {
+    g_last_launches = 0;
+    return CB_OK;
+  }
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return CB_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache)) return CB_EINVAL;
+  DeviceInfo di;
+  if (!device_info(&di)) return CB_ECUDA;
+  cudaError_t e = launch_kv_append(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_blocks, n_kv_heads,
+                                   head_dim, di.err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return CB_ECUDA;
+  g_last_launches = 1;
+  return CB_OK;
+}
+
+size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len, int n_q_heads,
+                                         int n_kv_heads, int head_dim, int block_size) {
+  if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
+      !shape_ok(n_q_heads, n_kv_heads, head_dim, block_size))
+    return 0;
+  return workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks).total;
+}
+
+int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
+                       int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
+                       const void* k_cache, const void* v_cache, int num_blocks, void* out, float scale,
+                       int n_q_heads, int n_kv_heads, int head_dim, int block_size, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!shape_ok(n_q_heads, n_kv_heads, head_dim, block_size)) return CB_EINVAL;
+  if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
+      max_blocks_per_seq < 1 || num_blocks <= 0 || !(scale > 0.f) || max_q_len > max_kv_len)
+    return CB_EINVAL;
+  if ((long long)num_blocks * n_kv_heads * kBlockSize >= (1LL << 31) - kBlockSize) return CB_EINVAL;
+  if (n_reqs == 0 || n_tokens == 0) {
+    g_last_launches = 0;
+    return CB_OK;
+  }
+  if (!q || !cu_q_lens || !ctx_lens || !block_tables || !k_cache || !v_cache || !out || !workspace) return CB_EINVAL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
+    return CB_EINVAL;
+  const WorkspaceLayout L = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8);
+  if (workspace_bytes < L.total) return CB_EWORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return CB_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  StepParams p{};
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const uint16_t*>(q);
+  p.cu_q_lens = cu_q_lens;
+  p.ctx_lens = ctx_lens;
+  p.block_tables = block_tables;
+  p.out = static_cast<uint16_t*>(out);
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_kv_len = max_kv_len;
+  p.n_reqs = n_reqs;
+  p.n_tokens = n_tokens;
+  p.num_blocks = num_blocks;
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.split_blocks = choose_split_blocks(n_reqs, max_kv_len, n_kv_heads, di.n_sms);
+  p.max_splits_total = L.max_splits_total;
+  p.counters = reinterpret_cast<int*>(ws + L.counters);
+  p.queue = reinterpret_cast<int*>(ws + L.queue);
+  p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  p.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
+  p.err = di.err;
+
+  CUtensorMap kmap, vmap;
+  if (!encode_cache_map(&kmap, k_cache, num_blocks, n_kv_heads, head_dim) ||
+      !encode_cache_map(&vmap, v_cache, num_blocks, n_kv_heads, head_dim))
+    return CB_ECUDA;
+  // split arrival counters and the work queue start at zero every call
+  if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
+  const int group = n_q_heads / n_kv_heads;
+  cudaError_t e;
+  if (max_q_len == 1) {
+    e = launch_decode(p, kmap, vmap, head_dim, group, di.n_sms, s);
+  } else {
+    CUtensorMap qmap;
+    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, group)) return CB_ECUDA;
+    e = launch_mixed(p, kmap, vmap, qmap, head_dim, group, di.n_sms, s);
+  }
+  if (e != cudaSuccess) return CB_ECUDA;
+  g_last_launches = 1;
+  return CB_OK;
+}
+
+int cb_last_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CB_ECUDA;
+  unsigned int bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_dev_error, sizeof(bits)) != cudaSuccess) return CB_ECUDA;
+  if (bits) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return CB_ECUDA;
+  }
+  if (bits & CB_DEVERR_TIMEOUT) return CB_ETIMEOUT;
+  if (bits) return CB_EDEVICE;
+  return CB_OK;
+}
+
+const char* cb_strerror(int code) {
+  switch (code) {
+    case CB_OK: return "ok";
+    case CB_EINVAL: return "invalid argument (size, shape, null or misaligned pointer)";
+    case CB_ECUDA: return "CUDA runtime or launch error";
+    case CB_EWORKSPACE: return "workspace too small";
+    case CB_EDEVICE: return "kernel found bad metadata (block id, slot or length out of range)";
+    case CB_ETIMEOUT: return "kernel wait timed out";
+    case CB_ESTATE: return "scheduler state error or capacity exceeded";
+    default: return "unknown error";
+  }
+}
+
+int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (!dst || !src || (bytes & 15) || !aligned16(dst) || !aligned16(src)) return CB_EINVAL;
+  DeviceInfo di;
+  if (!device_info(&di)) return CB_ECUDA;
+  if (launch_hbm_copy(dst, src, bytes, di.n_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CB_ECUDA;
+  g_last_launches = 1;
+  return CB_OK;
+}
+
+int cb_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal constants and launch interfaces shared by the library's translation
+// units.  Not part of the public C ABI (that is include/cbattn.h).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace cb {
+
+// Device error-word bits.
+constexpr unsigned CB_DEVERR_TIMEOUT = 1u;   // a bounded mbarrier wait ran out
+constexpr unsigned CB_DEVERR_BADBLOCK = 2u;  // block-table entry outside [0, num_blocks)
+constexpr unsigned CB_DEVERR_BADSLOT = 4u;   // slot outside the cache
+constexpr unsigned CB_DEVERR_BADLEN = 8u;    // lengths inconsistent with the table / launch
+
+// Longest a kernel waits on one mbarrier phase before giving up (wall clock).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+constexpr int kBlockSize = 16;     // tokens per physical KV block
+constexpr int kTileM = 128;        // query rows per tensor-core tile
+constexpr int kTileN = 128;        // keys per tensor-core tile
+constexpr int kMaxReqs = 2048;     // requests per step (plan arrays live in shared memory)
+constexpr int kMaxSplitBlocks = 32;  // decode split size limit (one warp-wide table load)
+
+// Everything a step's attention kernels read besides the tensor maps.
+struct StepParams {
+  const uint16_t* q;            // bf16 [n_tokens][Hq][A]
+  const int32_t* cu_q_lens;     // [n_reqs + 1]
+  const int32_t* ctx_lens;      // [n_reqs]
+  const int32_t* block_tables;  // [n_reqs][max_blocks_per_seq]
+  uint16_t* out;                // bf16 [n_tokens][Hq][A]
+  int max_blocks_per_seq;
+  int max_kv_len;               // caller's bound on ctx + q_len (sizes the partial buffers)
+  int n_reqs;
+  int n_tokens;
+  int num_blocks;
+  int n_q_heads;
+  int n_kv_heads;
+  float scale_log2;             // scale * log2(e): scores kept in the base-2 domain
+  int split_blocks;             // decode split size (blocks)
+  int max_splits_total;         // capacity of the partial buffers (splits)
+  // workspace
+  int* counters;                // [n_reqs * Hkv] split arrival counters (zeroed per call)
+  int* queue;                   // [4] work counters (zeroed per call)
+  float* part_ml;               // [max_splits_total * Hq * 2] (max, sum) per split and head
+  float* part_acc;              // [max_splits_total * Hq * A] unnormalised outputs per split
+  unsigned int* err;            // device error word
+};
+
+// Workspace carving (byte offsets), shared by the size query and the launcher.
+struct WorkspaceLayout {
+  size_t counters, queue, part_ml, part_acc, total;
+  int max_splits_total;
+};
+WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int split_blocks);
+int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms);
+
+// Kernel launchers (defined in the .cu files); return a cudaError_t.
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t* slots, int n_tokens,
+                             void* k_cache, void* v_cache, int num_blocks, int n_kv_heads, int head_dim,
+                             unsigned int* err, cudaStream_t stream);
+cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int head_dim,
+                          int group, int n_sms, cudaStream_t stream);
+cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const CUtensorMap& qmap, int head_dim, int group, int n_sms, cudaStream_t stream);
+cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
+
+}  // namespace cb

@@ -1,0 +1,285 @@
+// FCFS iteration-level continuous-batching scheduler with a paged block
+// allocator and recompute preemption.  Host only; produces each step's
+// attention metadata (request order, new tokens, stored tokens, block tables,
+// slot mapping).
+//
+// [KVN] Continuous Batching原理: every iteration retires finished requests,
+// admits new ones and steps every running request.  [KVN] 调度策略: FCFS order,
+// preemption when memory runs out.  [CB] Chunked prefill / Continuous batching:
+// prompts may run in chunks, and prefill and decode tokens share one ragged
+// batch bounded by a token budget.  [SM] PagedAttention: a request takes a new
+// block only when its last block is full.
+//
+// The per-step rules (the pages print no algorithm; this is the plain FCFS
+// reading):
+//  a. arrivals join the waiting queue (kept in arrival order);
+//  b. running requests with one position left (decoding) get 1 token each in
+//     arrival order; with no free block, the latest-arrived running request with
+//     nothing scheduled this step is preempted (possibly the request itself);
+//  c. running requests still prefilling get min(remaining, budget left) tokens,
+//     preempting only later-arrived unscheduled requests, else cut to what fits;
+//  d. waiting requests are admitted in order while budget is left, stopping at
+//     the first one that gets no token or was preempted in this step.
+// A preempted request frees all blocks, keeps its produced tokens and re-runs
+// prompt + produced tokens as a prefill later.  Free blocks are FIFO.
+#include <algorithm>
+#include <deque>
+#include <vector>
+
+#include "../../include/cbattn.h"
+
+namespace {
+
+enum State { kPending = 0, kWaiting = 1, kRunning = 2, kFinished = 3, kRejected = 4 };
+
+struct Req {
+  int rid, arrival, prompt, output;
+  int produced = 0, stored = 0, state = kPending, preemptions = 0;
+  std::vector<int> blocks;
+  int remaining() const { return prompt + produced - stored; }
+};
+
+struct Sched {
+  int num_blocks, bs, budget, max_batch;
+  std::deque<int> free_list;
+  std::vector<Req> reqs;
+  size_t next_pending = 0;
+  std::vector<int> waiting;   // request ids, ascending
+  std::vector<int> running;   // request ids, ascending
+  int now = 0;
+
+  int blocks_for(long long n) const { return (int)((n + bs - 1) / bs); }
+
+  void grow(Req& r, long long n_tokens) {
+    const int need = blocks_for(n_tokens) - (int)r.blocks.size();
+    for (int i = 0; i < need; ++i) {
+      r.blocks.push_back(free_list.front());
+      free_list.pop_front();
+    }
+  }
+  void release(Req& r) {
+    for (int b : r.blocks) free_list.push_back(b);
+    r.blocks.clear();
+  }
+  static void insert_sorted(std::vector<int>& v, int rid) { v.insert(std::lower_bound(v.begin(), v.end(), rid), rid); }
+  static void erase(std::vector<int>& v, int rid) {
+    auto it = std::lower_bound(v.begin(), v.end(), rid);
+    if (it != v.end() && *it == rid) v.erase(it);
+  }
+  void preempt(int rid) {
+    Req& r = reqs[rid];
+    release(r);
+    r.stored = 0;
+    r.state = kWaiting;
+    r.preemptions++;
+    erase(running, rid);
+    insert_sorted(waiting, rid);
+  }
+};
+
+}  // namespace
+
+struct cb_sched {
+  Sched s;
+};
+
+extern "C" {
+
+cb_sched* cb_sched_create(int num_blocks, int block_size, int token_budget, int max_batch, const int32_t* free_order) {
+  if (num_blocks <= 0 || block_size <= 0 || token_budget <= 0 || max_batch <= 0 || !free_order) return nullptr;
+  std::vector<char> seen(num_blocks, 0);
+  for (int i = 0; i < num_blocks; ++i) {
+    const int b = free_order[i];
+    if (b < 0 || b >= num_blocks || seen[b]) return nullptr;
+    seen[b] = 1;
+  }
+  cb_sched* h = new cb_sched();
+  h->s.num_blocks = num_blocks;
+  h->s.bs = block_size;
+  h->s.budget = token_budget;
+  h->s.max_batch = max_batch;
+  for (int i = 0; i < num_blocks; ++i) h->s.free_list.push_back(free_order[i]);
+  return h;
+}
+
+void cb_sched_destroy(cb_sched* h) { delete h; }
+
+int cb_sched_add_request(cb_sched* h, int arrival_step, int prompt_len, int output_len) {
+  if (!h || arrival_step < 0 || prompt_len < 1 || output_len < 1) return CB_EINVAL;
+  Sched& s = h->s;
+  if (!s.reqs.empty() && arrival_step < s.reqs.back().arrival) return CB_EINVAL;
+  Req r;
+  r.rid = (int)s.reqs.size();
+  r.arrival = arrival_step;
+  r.prompt = prompt_len;
+  r.output = output_len;
+  s.reqs.push_back(r);
+  return r.rid;
+}
+
+int cb_sched_done(const cb_sched* h) {
+  if (!h) return 1;
+  const Sched& s = h->s;
+  return s.next_pending == s.reqs.size() && s.waiting.empty() && s.running.empty();
+}
+
+int cb_sched_free_blocks(const cb_sched* h) { return h ? (int)h->s.free_list.size() : 0; }
+
+int cb_sched_request_info(const cb_sched* h, int req_id, int* produced, int* stored, int* preemptions, int* state) {
+  if (!h || req_id < 0 || req_id >= (int)h->s.reqs.size()) return CB_ESTATE;
+  const Req& r = h->s.reqs[req_id];
+  if (produced) *produced = r.produced;
+  if (stored) *stored = r.stored;
+  if (preemptions) *preemptions = r.preemptions;
+  if (state) *state = r.state;
+  return CB_OK;
+}
+
+int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
+                  int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
+                  int* n_tokens_out) {
+  if (!h || !req_ids || !q_lens || !ctx_lens || !cu_q_lens || !block_tables || !slot_mapping || !n_reqs_out ||
+      !n_tokens_out || max_blocks_per_seq < 1)
+    return CB_EINVAL;
+  Sched& s = h->s;
+  // a. arrivals
+  while (s.next_pending < s.reqs.size() && s.reqs[s.next_pending].arrival <= s.now) {
+    Req& r = s.reqs[s.next_pending++];
+    if (s.blocks_for((long long)r.prompt + r.output - 1) > s.num_blocks) {
+      r.state = kRejected;
+      continue;
+    }
+    r.state = kWaiting;
+    s.waiting.push_back(r.rid);
+  }
+  struct Item {
+    int rid, n, c;
+  };
+  std::vector<Item> sched;
+  std::vector<int> preempted;
+  std::vector<char> scheduled(s.reqs.size(), 0);
+  int budget = s.budget;
+  auto victim = [&](int after_rid) -> int {
+    for (auto it = s.running.rbegin(); it != s.running.rend(); ++it)
+      if (*it > after_rid && !scheduled[*it]) return *it;
+      else if (*it <= after_rid) break;
+    return -1;
+  };
+  auto full = [&] { return (int)sched.size() >= s.max_batch; };
+
+  // b. running decodes, arrival order
+  {
+    const std::vector<int> snap = s.running;
+    for (int rid : snap) {
+      if (budget == 0 || full()) break;
+      Req& r = s.reqs[rid];
+      if (r.state != kRunning || r.remaining() != 1) continue;
+      while (s.blocks_for((long long)r.stored + 1) - (int)r.blocks.size() > (int)s.free_list.size()) {
+        const int v = victim(rid - 1);           // includes rid itself
+        s.preempt(v);
+        preempted.push_back(v);
+        if (v == rid) break;
+      }
+      if (r.state != kRunning) continue;
+      s.grow(r, (long long)r.stored + 1);
+      sched.push_back({rid, 1, r.stored});
+      scheduled[rid] = 1;
+      budget -= 1;
+    }
+  }
+  // c. running prefills, arrival order
+  {
+    const std::vector<int> snap = s.running;
+    for (int rid : snap) {
+      if (budget == 0 || full()) break;
+      Req& r = s.reqs[rid];
+      if (r.state != kRunning || scheduled[rid] || r.remaining() <= 1) continue;
+      const int want = std::min(r.remaining(), budget);
+      while (s.blocks_for((long long)r.stored + want) - (int)r.blocks.size() > (int)s.free_list.size()) {
+        const int v = victim(rid);
+        if (v < 0) break;
+        s.preempt(v);
+        preempted.push_back(v);
+      }
+      const long long fit = (long long)(r.blocks.size() + s.free_list.size()) * s.bs - r.stored;
+      const int n = (int)std::min<long long>(want, fit);
+      if (n <= 0) continue;
+      s.grow(r, (long long)r.stored + n);
+      sched.push_back({rid, n, r.stored});
+      scheduled[rid] = 1;
+      budget -= n;
+    }
+  }
+  // d. admissions, queue order
+  while (!s.waiting.empty() && budget > 0 && !full()) {
+    const int rid = s.waiting.front();
+    if (std::find(preempted.begin(), preempted.end(), rid) != preempted.end()) break;
+    Req& r = s.reqs[rid];
+    const long long fit = (long long)s.free_list.size() * s.bs;
+    const int n = (int)std::min<long long>(std::min(r.remaining(), budget), fit);
+    if (n <= 0) break;
+    s.waiting.erase(s.waiting.begin());
+    r.state = kRunning;
+    Sched::insert_sorted(s.running, rid);
+    s.grow(r, (long long)r.stored + n);
+    sched.push_back({rid, n, r.stored});
+    scheduled[rid] = 1;
+    budget -= n;
+  }
+
+  // metadata
+  int rc = (int)preempted.size();
+  const int nb = (int)sched.size();
+  int tok = 0;
+  cu_q_lens[0] = 0;
+  for (int i = 0; i < nb; ++i) {
+    const Req& r = s.reqs[sched[i].rid];
+    req_ids[i] = sched[i].rid;
+    q_lens[i] = sched[i].n;
+    ctx_lens[i] = sched[i].c;
+    cu_q_lens[i + 1] = cu_q_lens[i] + sched[i].n;
+    int32_t* row = block_tables + (size_t)i * max_blocks_per_seq;
+    if ((int)r.blocks.size() > max_blocks_per_seq) rc = CB_ESTATE;
+    for (int b = 0; b < max_blocks_per_seq; ++b) row[b] = b < (int)r.blocks.size() ? r.blocks[b] : -1;
+    for (int p = sched[i].c; p < sched[i].c + sched[i].n; ++p)
+      slot_mapping[tok++] = (int64_t)r.blocks[p / s.bs] * s.bs + p % s.bs;
+  }
+  *n_reqs_out = nb;
+  *n_tokens_out = tok;
+
+  // the forward pass runs here; every scheduled request advances
+  for (const Item& it : sched) {
+    Req& r = s.reqs[it.rid];
+    r.stored += it.n;
+    if (r.stored == r.prompt + r.produced) r.produced++;
+    if (r.produced == r.output) {
+      r.state = kFinished;
+      s.release(r);
+      Sched::erase(s.running, it.rid);
+    }
+  }
+  s.now++;
+  return rc;
+}
+
+int cb_build_slot_mapping(const int32_t* q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
+                          int max_blocks_per_seq, int n_reqs, int block_size, int64_t* slot_mapping_out) {
+  if (!q_lens || !ctx_lens || !block_tables || !slot_mapping_out || n_reqs < 0 || block_size <= 0 ||
+      max_blocks_per_seq < 1)
+    return CB_EINVAL;
+  long long t = 0;
+  for (int r = 0; r < n_reqs; ++r) {
+    if (q_lens[r] < 0 || ctx_lens[r] < 0) return CB_EINVAL;
+    for (int i = 0; i < q_lens[r]; ++i) {
+      const long long p = (long long)ctx_lens[r] + i;
+      const long long lb = p / block_size;
+      if (lb >= max_blocks_per_seq) return CB_EINVAL;
+      const int e = block_tables[(size_t)r * max_blocks_per_seq + lb];
+      if (e < 0) return CB_EINVAL;
+      slot_mapping_out[t++] = (int64_t)e * block_size + p % block_size;
+    }
+  }
+  return CB_OK;
+}
+
+}  // extern "C"

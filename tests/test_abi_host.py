@@ -1,0 +1,100 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/cbattn.h declares, rejects bad arguments on the host before touching
+CUDA, and its pure-host functions (workspace sizing, slot mapping) agree with
+the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import paged as op
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib():
+    from paged_kv_cache_cb_gb300 import _lib as L
+    if not os.path.exists(L.LIB_PATH):
+        from paged_kv_cache_cb_gb300 import build
+        build.build()
+    return L
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "cbattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for must in ("cb_kv_append", "cb_paged_attention", "cb_paged_attention_workspace_size", "cb_last_error",
+                 "cb_strerror", "cb_sched_create", "cb_sched_step", "cb_build_slot_mapping"):
+        assert must in syms
+
+
+def test_library_exports_every_declared_symbol():
+    L = _lib()
+    lib = ctypes.CDLL(L.LIB_PATH)
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+    bound = {name for name, _, _ in L.SIGNATURES}
+    assert set(declared_symbols()) == bound, "binding must cover exactly the header's entry points"
+
+
+def test_host_side_argument_checks():
+    L = _lib().lib()
+    V = ctypes.c_void_p
+    dummy = V(4096)
+    # unsupported head_dim / block_size / group and bad sizes are rejected before any CUDA call
+    assert L.cb_kv_append(dummy, dummy, dummy, 4, dummy, dummy, 8, 2, 96, 16, None) == -1
+    assert L.cb_kv_append(dummy, dummy, dummy, 4, dummy, dummy, 8, 2, 128, 32, None) == -1
+    args = lambda **kw: [kw.get(k, v) for k, v in [
+        ("q", dummy), ("cu", dummy), ("ctx", dummy), ("bt", dummy), ("maxb", 4), ("nr", 2), ("nt", 3),
+        ("mq", 2), ("mkv", 40), ("kc", dummy), ("vc", dummy), ("nb", 16), ("out", dummy), ("scale", 0.1),
+        ("hq", 4), ("hk", 2), ("a", 128), ("bs", 16), ("ws", dummy), ("wsb", 1 << 30), ("s", None)]]
+    assert L.cb_paged_attention(*args(hq=6, hk=4)) == -1            # Hq % Hkv != 0
+    assert L.cb_paged_attention(*args(hq=32, hk=2)) == -1           # group 16 unsupported
+    assert L.cb_paged_attention(*args(a=96)) == -1
+    assert L.cb_paged_attention(*args(bs=8)) == -1
+    assert L.cb_paged_attention(*args(nr=5000)) == -1               # more than CB_MAX_REQS
+    assert L.cb_paged_attention(*args(scale=0.0)) == -1
+    assert L.cb_paged_attention(*args(q=None)) == -1
+    assert L.cb_paged_attention(*args(q=V(4100))) == -1             # not 16-byte aligned
+    assert L.cb_paged_attention(*args(wsb=16)) == -3                # workspace too small
+    assert L.cb_paged_attention(*args(nr=0)) == 0                   # empty batch: nothing to do
+    assert L.cb_strerror(-3) == b"workspace too small"
+
+
+def test_workspace_size_grows_with_requests_and_context():
+    L = _lib()
+    f = L.cb_paged_attention_workspace_size
+    a = f(64, 64, 1, 4097, 32, 32, 128, 16)
+    assert a > 0
+    assert f(128, 128, 1, 4097, 32, 32, 128, 16) > a
+    assert f(64, 64, 1, 8193, 32, 32, 128, 16) > a
+    assert f(64, 64, 1, 4097, 32, 32, 96, 16) == 0
+    # bound: n_reqs * ceil(ceil(kv/16)/8) splits of (A + 2) floats per q head, plus counters
+    splits = 64 * -(-(-(-4097 // 16)) // 8)
+    assert a >= splits * 32 * (128 + 2) * 4
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_host_slot_mapping_matches_oracle(seed):
+    L = _lib()
+    shape = wl.random_step(seed, n_reqs=9, max_ctx=70, max_q=20, n_q_heads=4, n_kv_heads=2, head_dim=64)
+    bt = wl.block_tables(shape)
+    got = L.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, bt, shape.block_size)
+    want = op.slot_mapping(bt, shape.q_lens, shape.ctx_lens, shape.block_size)
+    assert got.dtype == np.int64 and np.array_equal(got, want)
+
+
+def test_host_slot_mapping_rejects_short_tables():
+    L = _lib()
+    with pytest.raises(L.CBError):
+        L.cb_build_slot_mapping([3], [30], np.array([[1, 2]], np.int32), 16)   # needs 3 blocks
+    with pytest.raises(L.CBError):
+        L.cb_build_slot_mapping([1], [0], np.array([[-1]], np.int32), 16)

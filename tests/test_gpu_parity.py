@@ -1,0 +1,240 @@
+"""GPU parity: the C-ABI path (cb_kv_append + cb_paged_attention on GB300)
+against the fp64 oracle on the same seeded inputs.
+
+Cache append and block-table indexing: bit-exact.  Attention: max abs error
+<= 2e-2 and max abs error / max |reference| <= 1e-2 (bf16 inputs and outputs,
+fp32 accumulation)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import L, assert_close, device_step, f64, oracle_step, sampled_request_oracle
+from oracle import paged as op
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L().lib()
+
+
+# ------------------------------------------------------------------ append
+@pytest.mark.parametrize("shape", [wl.tiny(), wl.random_step(3, 12, 90, 40, 8, 2, 128),
+                                   wl.random_step(4, 7, 33, 17, 4, 4, 64)], ids=lambda s: s.name)
+def test_append_is_bit_exact_including_untouched_slots(shape):
+    inp = wl.step_inputs_cpu(shape)
+    lib = L()
+    slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, inp["block_tables"], shape.block_size)
+    assert np.array_equal(slots, op.slot_mapping(inp["block_tables"], shape.q_lens, shape.ctx_lens, shape.block_size))
+    kc, vc = inp["k_pool"].cuda(), inp["v_pool"].cuda()
+    lib.cb_kv_append(inp["k_new"].cuda(), inp["v_new"].cuda(), torch.from_numpy(slots).cuda(), kc, vc)
+    assert lib.cb_last_error() == 0
+    want_k = inp["k_pool"].view(torch.int16).numpy().copy()
+    want_v = inp["v_pool"].view(torch.int16).numpy().copy()
+    op.append_rows(want_k, inp["k_new"].view(torch.int16).numpy(), slots, shape.block_size)
+    op.append_rows(want_v, inp["v_new"].view(torch.int16).numpy(), slots, shape.block_size)
+    assert np.array_equal(kc.cpu().view(torch.int16).numpy(), want_k)
+    assert np.array_equal(vc.cpu().view(torch.int16).numpy(), want_v)
+
+
+def test_append_negative_slot_skips_and_bad_slot_is_reported():
+    shape = wl.tiny()
+    inp = wl.step_inputs_cpu(shape)
+    lib = L()
+    slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, inp["block_tables"], shape.block_size)
+    slots[1] = -1
+    kc, vc = inp["k_pool"].cuda(), inp["v_pool"].cuda()
+    lib.cb_kv_append(inp["k_new"].cuda(), inp["v_new"].cuda(), torch.from_numpy(slots).cuda(), kc, vc)
+    assert lib.cb_last_error() == 0
+    want = inp["k_pool"].view(torch.int16).numpy().copy()
+    op.append_rows(want, inp["k_new"].view(torch.int16).numpy(), slots, shape.block_size)
+    assert np.array_equal(kc.cpu().view(torch.int16).numpy(), want)
+    slots[0] = shape.num_blocks * shape.block_size + 5          # outside the cache: skipped, flagged
+    lib.cb_kv_append(inp["k_new"].cuda(), inp["v_new"].cuda(), torch.from_numpy(slots).cuda(), kc, vc)
+    assert lib.cb_last_error() == lib.CB_EDEVICE
+    assert lib.cb_last_error() == 0                               # the status is cleared once read
+
+
+# ------------------------------------------------------------------ attention, small
+def _parity(shape, scale=None):
+    inp = wl.step_inputs_cpu(shape)
+    out, _, _, _ = device_step(shape, inp, scale=scale)
+    ref = oracle_step(shape, inp, scale=scale)
+    return assert_close(f64(out), ref, shape.name)
+
+
+def test_tiny_mixed_batch():
+    """Two decodes (37 and 100 stored), the second chunk of a 7-token prompt cut at 4,
+    a fresh 20-token prefill; MHA 4 heads, head_dim 64."""
+    _parity(wl.tiny())
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_decode_only_split_k(group, head_dim):
+    base = wl.random_step(10 + group, n_reqs=9, max_ctx=1500, max_q=1, n_q_heads=8, n_kv_heads=8 // group,
+                          head_dim=head_dim, p_decode=1.0)
+    ctx = list(base.ctx_lens)
+    ctx[0], ctx[1], ctx[2] = 0, 15, 2047        # one key; block boundary; many splits with a ragged tail
+    _parity(wl.scaled(base, ctx_lens=ctx, num_blocks=base.num_blocks + 200))
+
+
+@pytest.mark.parametrize("group", [1, 4, 8])
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_chunked_prefill_tiles(group, head_dim):
+    """Prefill chunks spanning several 128-row query tiles and 128-key tiles with
+    ragged tails, after stored prefixes of various lengths (0, mid-block, long)."""
+    hq = 8
+    shape = wl.StepShape(f"prefill_g{group}_a{head_dim}", hq, hq // group, head_dim, 16, 200,
+                         q_lens=(300, 129, 2, 77), ctx_lens=(200, 0, 333, 1000), seed=group * 7 + head_dim)
+    _parity(shape)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_mixed_steps(seed):
+    group = [1, 2, 4, 8][seed % 4]
+    head_dim = [64, 128][seed % 2]
+    shape = wl.random_step(100 + seed, n_reqs=11, max_ctx=700, max_q=150, n_q_heads=8, n_kv_heads=8 // group,
+                           head_dim=head_dim, p_decode=0.6)
+    _parity(shape)
+
+
+def test_scale_argument_is_honoured():
+    _parity(wl.tiny(), scale=0.05)
+
+
+def test_chunked_equals_unchunked_on_gpu():
+    """[CB] Chunked prefill: a 7-token prompt run as chunks (4 then 3) gives the
+    same outputs as one 7-token prefill, through the paged cache."""
+    lib = L()
+    hq, hk, a, bs = 4, 4, 64, 16
+    rng = np.random.default_rng(0)
+    q = torch.from_numpy(rng.standard_normal((7, hq, a), dtype=np.float32)).to(torch.bfloat16).cuda()
+    k = torch.from_numpy(rng.standard_normal((7, hk, a), dtype=np.float32)).to(torch.bfloat16).cuda()
+    v = torch.from_numpy(rng.standard_normal((7, hk, a), dtype=np.float32)).to(torch.bfloat16).cuda()
+    table = np.array([[3]], np.int32)
+
+    def run(chunks):
+        kc = torch.zeros(8, hk, bs, a, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        outs = []
+        start = 0
+        for n in chunks:
+            slots = lib.cb_build_slot_mapping([n], [start], table, bs)
+            lib.cb_kv_append(k[start:start + n], v[start:start + n], torch.from_numpy(slots).cuda(), kc, vc)
+            ws = torch.empty(lib.cb_paged_attention_workspace_size(1, n, n, start + n, hq, hk, a, bs),
+                             dtype=torch.uint8, device="cuda")
+            o = torch.empty(n, hq, a, dtype=torch.bfloat16, device="cuda")
+            lib.cb_paged_attention(q[start:start + n].contiguous(), torch.tensor([0, n], dtype=torch.int32).cuda(),
+                                   torch.tensor([start], dtype=torch.int32).cuda(), torch.from_numpy(table).cuda(),
+                                   kc, vc, o, 1 / math.sqrt(a), ws, max(n, 2), start + n)
+            outs.append(o)
+            start += n
+        assert lib.cb_last_error() == 0
+        return torch.cat(outs).float().cpu().numpy()
+
+    full, chunked = run([7]), run([4, 3])
+    assert np.abs(full - chunked).max() <= 1e-2
+
+
+def test_outputs_are_deterministic():
+    shape = wl.random_step(7, n_reqs=10, max_ctx=3000, max_q=100, n_q_heads=8, n_kv_heads=2, head_dim=128)
+    inp = wl.step_inputs_cpu(shape)
+    o1 = device_step(shape, inp)[0]
+    o2 = device_step(shape, inp)[0]
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_batch_and_zero_length_requests():
+    lib = L()
+    shape = wl.StepShape("zero_q", 4, 2, 64, 16, 40, q_lens=(0, 3, 0, 1), ctx_lens=(10, 5, 0, 20), seed=1)
+    _parity(shape)
+    # an empty step launches nothing and succeeds
+    q = torch.empty(0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    lib.cb_paged_attention(q, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                           torch.zeros(0, dtype=torch.int32, device="cuda"),
+                           torch.zeros(0, 1, dtype=torch.int32, device="cuda"),
+                           torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16, device="cuda"),
+                           torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16, device="cuda"), q, 0.125,
+                           torch.empty(16, dtype=torch.uint8, device="cuda"), 1, 1)
+    assert lib.cb_last_launch_count() == 0
+
+
+def test_block_and_tile_boundaries():
+    """Lengths at exact multiples of the block (16) and tile (128) sizes and one past."""
+    shape = wl.StepShape("bounds", 8, 2, 128, 16, 300, q_lens=(1, 1, 128, 129, 16, 1),
+                         ctx_lens=(127, 128, 128, 127, 112, 255), seed=5)
+    _parity(shape)
+
+
+def test_bad_block_id_is_reported_not_read():
+    shape = wl.tiny()
+    inp = wl.step_inputs_cpu(shape)
+    inp["block_tables"] = inp["block_tables"].copy()
+    inp["block_tables"][1, 2] = shape.num_blocks + 1000      # decode request 1 reads it
+    inp["block_tables"][3, 0] = -7                           # prefill request 3 reads it
+    lib = L()
+    _, _, _, status = device_step(shape, inp, check=False)
+    assert status == lib.CB_EDEVICE
+
+
+def test_workspace_too_small_is_rejected():
+    shape = wl.tiny()
+    inp = wl.step_inputs_cpu(shape)
+    with pytest.raises(L().CBError):
+        device_step(shape, inp, ws_extra=-64)
+
+
+def test_max_requests():
+    """CB_MAX_REQS decode requests with short contexts in one step."""
+    lib = L()
+    n = lib.CB_MAX_REQS
+    rng = np.random.default_rng(3)
+    ctx = tuple(int(c) for c in rng.integers(0, 40, size=n))
+    shape = wl.StepShape("max_reqs", 4, 1, 64, 16, sum(-(-(c + 1) // 16) for c in ctx) + 4,
+                         q_lens=(1,) * n, ctx_lens=ctx, seed=9)
+    _parity(shape)
+
+
+# ------------------------------------------------------------------ full-size, sampled
+def _full_size(shape, sample, rows_per_req=None):
+    inp = wl.step_inputs_device(shape, "cuda")
+    out, _, _, _ = device_step(shape, inp)
+    cu = np.concatenate([[0], np.cumsum(shape.q_lens)])
+    for r in sample:
+        rows = None
+        if rows_per_req and shape.q_lens[r] > rows_per_req:
+            rng = np.random.default_rng(r)
+            rows = sorted(set(rng.choice(shape.q_lens[r], rows_per_req - 2, replace=False).tolist())
+                          | {0, shape.q_lens[r] - 1})
+        ref, rows = sampled_request_oracle(shape, inp, r, rows)
+        got = f64(out[cu[r]:cu[r + 1]])[rows]
+        assert_close(got, ref, f"{shape.name} request {r}")
+    del inp, out
+    torch.cuda.empty_cache()
+
+
+def test_full_size_decode_llama7b_layer():
+    """64 decodes, MHA 32 x 128, contexts 512..4096, 20 GB pool: 6 sampled requests."""
+    shape = wl.decode()
+    order = np.argsort(shape.ctx_lens)
+    _full_size(shape, [int(order[0]), int(order[-1]), 0, 17, 40, 63])
+
+
+def test_full_size_mixed_gqa_step():
+    """48 decodes + two 512-token chunks (after 1024 and 3072 stored), GQA 32/8."""
+    shape = wl.mixed()
+    _full_size(shape, [0, 11, 47, 48, 49], rows_per_req=12)
+
+
+def test_full_size_long_context_chunk():
+    """Step 15 of a 32768-token prompt in 2048-token chunks (30720 stored) + 16 decodes at 8207."""
+    shape = wl.long(15)
+    _full_size(shape, [0, 15, 16], rows_per_req=6)
