@@ -37,15 +37,15 @@ import workloads as wl  # noqa: E402
 METRIC = "mixed-step attention tokens/s; decode KV GB/s as % of measured HBM peak"
 UNIT = "tokens/s"
 WORKLOADS = {
-    "decode": (lambda seed: wl.decode(seed=seed),
+    "decode": (lambda seed, pool=20: wl.decode(seed=seed, pool_bytes=pool * wl.GB),
                "decode: 64 requests, ctx U[512,4096], MHA 32x128 (Llama-2-7B layer), bf16, block 16, 20 GB pool"),
-    "mixed": (lambda seed: wl.mixed(seed=seed),
+    "mixed": (lambda seed, pool=20: wl.mixed(seed=seed, pool_bytes=pool * wl.GB),
               "mixed: 48 decodes ctx U[256,8192] + 2x512-token chunks after 1024/3072, GQA 32/8 x128, bf16"),
-    "mixed_budget": (lambda seed: wl.mixed(seed=seed, budget_variant=True),
+    "mixed_budget": (lambda seed, pool=20: wl.mixed(seed=seed, budget_variant=True, pool_bytes=pool * wl.GB),
                      "mixed, 560-token budget: 48 decodes + one 512-token chunk after 1024, GQA 32/8 x128"),
-    "long": (lambda seed: wl.long(15, seed=seed),
+    "long": (lambda seed, pool=20: wl.long(15, seed=seed, pool_bytes=pool * wl.GB),
              "long: 2048-token chunk after 30720 stored (step 15 of a 32768 prompt) + 16 decodes at 8207, GQA 32/8"),
-    "tiny": (lambda seed: wl.tiny(seed=seed), "tiny: 4 requests (37,1),(100,1),(4,3),(0,20), MHA 4x64"),
+    "tiny": (lambda seed, pool=20: wl.tiny(seed=seed), "tiny: 4 requests (37,1),(100,1),(4,3),(0,20), MHA 4x64"),
 }
 KERNEL_SOURCES = ["cb_common.cuh", "cb_decode_item.cuh", "cb_decode.cu", "cb_mixed.cu", "cb_api.cu"]
 
@@ -456,14 +456,18 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-gb", type=float, default=20.0,
+                    help="K+V block pool size (blocks stay randomly scattered over it)")
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     make, desc = WORKLOADS[args.workload]
+    if args.pool_gb != 20.0:
+        desc = desc.replace("20 GB pool", f"{args.pool_gb:g} GB pool") + f" (pool {args.pool_gb:g} GB)"
     if args.impl == "reference":
-        run_reference(args, make(args.seed), desc, world, rank)
+        run_reference(args, make(args.seed, args.pool_gb), desc, world, rank)
         return
     # weak scaling: each rank runs its own batch of the same workload (its own seed)
-    run_ours(args, make(args.seed + rank), desc, world, rank, local)
+    run_ours(args, make(args.seed + rank, args.pool_gb), desc, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -26,12 +26,14 @@ def cu_of(q_lens):
     return np.concatenate([[0], np.cumsum(np.asarray(q_lens, np.int64))]).astype(np.int32)
 
 
-def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True):
-    """Append the step's new K/V and run attention; returns (out, k_cache, v_cache, status)."""
+def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True, attn_tables=None):
+    """Append the step's new K/V and run attention; returns (out, k_cache, v_cache, status).
+    ``attn_tables`` replaces the block tables that attention reads (the append
+    still uses the slots of ``inp["block_tables"]``)."""
     lib = L()
     scale = scale if scale is not None else 1.0 / math.sqrt(shape.head_dim)
-    bt = inp["block_tables"]
-    slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, bt, shape.block_size)
+    slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, inp["block_tables"], shape.block_size)
+    bt = inp["block_tables"] if attn_tables is None else attn_tables
     k_cache = inp["k_pool"].to(dev).clone() if inp["k_pool"].device.type == "cpu" else inp["k_pool"]
     v_cache = inp["v_pool"].to(dev).clone() if inp["v_pool"].device.type == "cpu" else inp["v_pool"]
     q = inp["q"].to(dev)

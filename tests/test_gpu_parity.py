@@ -177,12 +177,16 @@ def test_block_and_tile_boundaries():
 def test_bad_block_id_is_reported_not_read():
     shape = wl.tiny()
     inp = wl.step_inputs_cpu(shape)
-    inp["block_tables"] = inp["block_tables"].copy()
-    inp["block_tables"][1, 2] = shape.num_blocks + 1000      # decode request 1 reads it
-    inp["block_tables"][3, 0] = -7                           # prefill request 3 reads it
+    bad = inp["block_tables"].copy()
+    bad[1, 2] = shape.num_blocks + 1000      # decode request 1 reads it
+    bad[3, 0] = -7                           # prefill request 3 reads it
     lib = L()
-    _, _, _, status = device_step(shape, inp, check=False)
+    out, _, _, status = device_step(shape, inp, check=False, attn_tables=bad)
     assert status == lib.CB_EDEVICE
+    # the requests that do not touch a bad entry are still right
+    ref = oracle_step(shape, inp)
+    assert_close(f64(out[0:1]), ref[0:1], "request 0")
+    assert_close(f64(out[2:5]), ref[2:5], "request 2")
 
 
 def test_workspace_too_small_is_rejected():
