@@ -307,7 +307,7 @@ def run_ours(args, shape, desc, world, rank, local):
 
     # HBM copy probe in the same process (context for the measured peak)
     copy_gbs = None
-    if rank == 0:
+    if rank == 0 and not args.no_copy_probe:
         nb = 4 << 30
         a_ = torch.empty(nb, dtype=torch.uint8, device=dev)
         b_ = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -321,6 +321,7 @@ def run_ours(args, shape, desc, world, rank, local):
         torch.cuda.synchronize()
         copy_gbs = 2 * nb * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e9
         del a_, b_
+        torch.cuda.empty_cache()
 
     # ---- device-resident timed region
     sampler = ClockSampler(local) if rank == 0 else None
@@ -456,6 +457,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-probe", action="store_true", help="skip the in-process HBM copy probe")
     ap.add_argument("--pool-gb", type=float, default=20.0,
                     help="K+V block pool size (blocks stay randomly scattered over it)")
     args = ap.parse_args(argv)
