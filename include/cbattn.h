@@ -122,6 +122,39 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
                                          int n_q_heads, int n_kv_heads, int head_dim, int block_size);
 
+/* ---------------------------------------------------------------- no-allocation variant
+ * The pages have no counterpart: this exists for callers that cannot allocate
+ * device memory when they run a step -- hosts whose device memory is owned by
+ * an arena or custom allocator that this library cannot see (a plugin may not
+ * call cudaMalloc behind its host's back), and latency-bound serving loops that
+ * forbid allocation because it can synchronise the device and has unbounded
+ * latency.
+ *
+ * Same arguments, semantics and errors as cb_paged_attention, minus the
+ * workspace: the scratch (split-K partials and counters) comes from one
+ * library-owned device array of CB_NOALLOC_SCRATCH_BYTES, held on every GPU that
+ * loads the library until the process exits.  Nothing is allocated per call.
+ *  - Sizes whose cb_paged_attention_workspace_size(...) exceeds
+ *    CB_NOALLOC_SCRATCH_BYTES are rejected with CB_EWORKSPACE before anything
+ *    is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - The counters that must start at zero are cleared by every call (an async
+ *    memset on `stream`); the partial results are fully rewritten.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents: calls that may overlap on the GPU (different streams without
+ *    ordering between them) race and give undefined results.  Serialise them,
+ *    e.g. by issuing them on one stream.
+ */
+#define CB_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+int cb_paged_attention_noalloc(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                               const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                               int max_q_len, int max_kv_len, const void* k_cache, const void* v_cache,
+                               int num_blocks, void* out, float scale, int n_q_heads, int n_kv_heads,
+                               int head_dim, int block_size, void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word.
  * Returns CB_OK, CB_EDEVICE, CB_ETIMEOUT or CB_ECUDA. */
 int cb_last_error(void* stream);

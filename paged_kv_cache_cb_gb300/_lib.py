@@ -28,6 +28,8 @@ SIGNATURES = [
     ("cb_paged_attention", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                     _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     ("cb_paged_attention_workspace_size", _c_size, [_c_int] * 8),
+    ("cb_paged_attention_noalloc", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                            _c_int, _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp]),
     ("cb_last_error", _c_int, [_vp]),
     ("cb_strerror", ctypes.c_char_p, [_c_int]),
     ("cb_hbm_copy", _c_int, [_vp, _vp, _c_size, _vp]),
@@ -145,6 +147,38 @@ def cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, o
                                   int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs, pw,
                                   workspace.numel(), _stream(stream))
     _check("cb_paged_attention", rc)
+
+
+CB_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def cb_paged_attention_noalloc(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, out, scale, max_q_len,
+                               max_kv_len, stream=None):
+    """cb_paged_attention without a workspace argument: for callers that cannot
+    allocate device memory when they run a step.  Its scratch is the library's
+    fixed device array (CB_NOALLOC_SCRATCH_BYTES); steps that need more are
+    rejected (CBError, CB_EWORKSPACE).  Calls that overlap on the GPU share that
+    array and race."""
+    import torch
+    bf = torch.bfloat16
+    pq = _dev(q, bf, "q", 3)
+    po = _dev(out, bf, "out", 3)
+    pcu = _dev(cu_q_lens, torch.int32, "cu_q_lens", 1)
+    pctx = _dev(ctx_lens, torch.int32, "ctx_lens", 1)
+    pbt = _dev(block_tables, torch.int32, "block_tables", 2)
+    ck = _dev(k_cache, bf, "k_cache", 4)
+    cv = _dev(v_cache, bf, "v_cache", 4)
+    n_tok, hq, a = q.shape
+    n_reqs = ctx_lens.numel()
+    if out.shape != q.shape or cu_q_lens.numel() != n_reqs + 1 or block_tables.shape[0] != n_reqs:
+        raise ValueError("shape mismatch")
+    nb, hk, bs, a2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or a2 != a:
+        raise ValueError("cache shape mismatch")
+    rc = lib().cb_paged_attention_noalloc(pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok, int(max_q_len),
+                                          int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs,
+                                          _stream(stream))
+    _check("cb_paged_attention_noalloc", rc)
 
 
 def cb_last_error(stream=None):
