@@ -153,7 +153,8 @@ struct alignas(1024) DecWarpSmem {
 
 // Runs one decode work item.  Returns false if a wait timed out (the warp must
 // stop).  `parity` carries each stage's next mbarrier parity across items.
-template <int A, int G, int NST>
+// QKU: unroll factor of the QK chunk loop (register pressure vs. ILP).
+template <int A, int G, int NST, int QKU>
 __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
                             DecWarpSmem<A, G, NST>& S, uint32_t& parity, int r, int g, int split, int nsplit,
                             int split_slot0) {
@@ -239,7 +240,7 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
       float part[G][2];
 #pragma unroll
       for (int j = 0; j < G; ++j) part[j][0] = part[j][1] = 0.f;
-#pragma unroll
+#pragma unroll QKU
       for (int ci = 0; ci < CPL; ++ci) {
         const int cc = hf_l * CPL + ci;        // logical 16-byte chunk of the row
         const int half = cc >> 3, pos = cc & 7;
@@ -401,7 +402,7 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
 
 // Pull decode items from the global queue until none is left.  `dec` and
 // `spl` are the plan's prefix arrays.
-template <int A, int G, int NST>
+template <int A, int G, int NST, int QKU = A / 16>
 __device__ void decode_worker(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               DecWarpSmem<A, G, NST>& S, const int* dec, const int* spl) {
   const int lane = threadIdx.x & 31;
@@ -421,7 +422,7 @@ __device__ void decode_worker(const StepParams& P, const CUtensorMap* kmap, cons
     const int nsplit = spl[r + 1] - spl[r];
     const int rem = item - dec[r];
     const int split = rem / P.n_kv_heads, g = rem - split * P.n_kv_heads;
-    if (!decode_item<A, G, NST>(P, kmap, vmap, S, parity, r, g, split, nsplit, spl[r])) break;
+    if (!decode_item<A, G, NST, QKU>(P, kmap, vmap, S, parity, r, g, split, nsplit, spl[r])) break;
   }
 }
 

@@ -1,33 +1,38 @@
 // One launch for a mixed continuous-batching step ([CB] Continuous batching:
 // prefill chunks and decode tokens in one ragged batch).
 //
-// Persistent grid, one CTA (6 warps) per SM.  Phase 1 runs this CTA's share of
-// the prefill tiles (requests with more than one new token, [CB] Chunked
-// prefill) on the tensor cores; phase 2 turns all six warps into decode
-// workers that pull (request, KV head, split) items from a global counter, so
-// CTAs that finish their prefill share early absorb more decode work.
+// Persistent grid, one CTA (10 warps) per SM.  Phase 1 runs this CTA's share of
+// the prefill work (requests with more than one new token, [CB] Chunked
+// prefill) on the tensor cores; phase 2 turns eight warps into decode workers
+// that pull (request, KV head, split) items from a global counter, so CTAs that
+// finish their prefill share early absorb more decode work.
 //
-// Prefill tile = (request r, KV head g, query tile): 128 rows = 128/G new tokens
-// x the G query heads of group g (GQA heads packed into the M dimension, all
-// sharing KV head g).  Row i is token i/G, head g*G + i%G, at absolute position
-// ctx + token; it sees keys 0..ctx+token (the chunk's causal mask shifted by the
-// stored prefix).  Keys stream in tiles of 128 (8 physical blocks of 16, each
-// fetched through the block table by two 2-D TMA boxes of 16 rows x 64 columns,
-// 128-byte swizzle, straight into the canonical K-major layout).
+// Prefill item = (request r, KV head g, pair of query tiles A and B).  A query
+// tile is 128 rows = 128/G new tokens x the G query heads of group g (GQA heads
+// packed into the MMA's M dimension, all sharing KV head g); tile B holds the
+// next 128/G tokens.  Row i of a tile is token i/G, head g*G + i%G, at absolute
+// position ctx + token; it sees keys 0..ctx+token (the chunk's causal mask
+// shifted by the stored prefix).  Keys stream in tiles of 128 (8 physical
+// blocks of 16, each fetched through the block table as two 2-D TMA boxes of 16
+// rows x 64 columns, 128-byte swizzle, straight into the canonical K-major
+// layout); both query tiles use every K and V tile.
 //
-// Warp roles:  warps 0-3  softmax: thread i owns row i.  Reads S from tensor
-//                         memory (TMEM), masks, keeps the running max m and sum
-//                         l in base 2, writes P (bf16) to shared memory, rescales
-//                         the O accumulator in TMEM when the max grows by more
-//                         than 2^8 (lazy rescale: exact, the final O/l uses the
-//                         same reference max), and finally writes O/l.
-//              warp 4     TMA producer: Q tile, then K/V tiles into 2 stages.
-//              warp 5     MMA issuer: S = Q K^T into one of two TMEM buffers
-//                         (tcgen05.mma kind::f16, M=128 N=128 K=16 steps), and
-//                         O += P V into the TMEM accumulator (V as MN-major
-//                         operand); completion via tcgen05.commit -> mbarrier.
-// S(j+1) is issued before O += P(j) V(j), so the tensor core computes the next
-// score tile while the softmax warps work on the current one.
+// Tensor memory (512 columns): S_A|P_A [0,128), S_B|P_B [128,256), O_A, O_B.
+// P (bf16) is written over the first half of its own S columns and consumed as
+// the A operand of O += P V straight from tensor memory.
+//
+// Warp roles:  warps 0-3  softmax of tile A, warps 4-7 softmax of tile B:
+//                         thread = row.  Reads S from TMEM, masks, keeps the
+//                         running max m (base 2, scale folded in) and sum l,
+//                         writes P, rescales O in TMEM only when the max grows
+//                         by more than 2^8 (lazy rescale: exact, the final O/l
+//                         uses the same reference max), finally writes O/l.
+//              warp 8     TMA producer: Q pair, K tiles and V tiles into
+//                         separate 2-stage rings; 16 lanes issue the boxes.
+//              warp 9     MMA issuer (one lane): per key tile
+//                         PV_A(j), PV_B(j), S_A(j+1), S_B(j+1)
+//                         so one tile's softmax overlaps the other tile's MMAs.
+// Every wait is bounded.
 #include "cb_decode_item.cuh"
 
 namespace cb {
@@ -35,21 +40,25 @@ namespace cb {
 namespace {
 
 constexpr int kSmemLimit = 232448;
-constexpr int kNumThreads = 192;
-constexpr int kDecStages = 3;
+constexpr int kNumThreads = 320;
+constexpr int kDecWarps = 8;
+constexpr int kDecStages = 2;
 
 template <int A>
 struct PrefillTiles {
   static constexpr int kHalves = A / 64;
-  static constexpr int kHalfBytes = 128 * 128;     // 128 rows x 128 bytes
-  uint8_t q[kHalves][128][128];
-  uint8_t k[2][kHalves][128][128];
-  uint8_t v[2][kHalves][128][128];
-  uint8_t p[2][128][128];                          // P: [key half][row][64 keys]
+  static constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kHalfBytes;     // one 128-row tile of Q, K or V
+  uint8_t q[2][kHalves][128][128];                             // query tiles A, B
+  uint8_t k[2][kHalves][128][128];                             // key ring
+  uint8_t v[2][kHalves][128][128];                             // value ring
 };
 
 struct MixedCtl {
-  uint64_t q_full, q_empty, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, o_free, drain;
+  uint64_t q_full, q_empty;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];        // per query tile (A, B)
+  uint64_t drain;
   uint32_t tmem_base;
   volatile int abort;
   int scratch[96];
@@ -59,18 +68,20 @@ struct PreItem {
   int r, g, q0, ctx, tok_lo, tok_hi, kv_hi, nkt;
 };
 
-__device__ __forceinline__ PreItem pre_item(const StepParams& P, const int* pre, int item, int tok_per_tile) {
+// Item -> (request, KV head, token range of the tile pair).  Pairs of the same
+// request are numbered from its last tokens (most keys) down.
+__device__ __forceinline__ PreItem pre_item(const StepParams& P, const int* pre, int item, int tok_per_pair) {
   PreItem I;
   I.r = find_request(pre, P.n_reqs, item);
   const int rem = item - pre[I.r];
   I.q0 = __ldg(P.cu_q_lens + I.r);
   const int q_len = __ldg(P.cu_q_lens + I.r + 1) - I.q0;
   I.ctx = __ldg(P.ctx_lens + I.r);
-  const int n_qt = (q_len + tok_per_tile - 1) / tok_per_tile;
-  const int qt = n_qt - 1 - rem / P.n_kv_heads;    // heaviest (last) query tiles first
+  const int n_pairs = (q_len + tok_per_pair - 1) / tok_per_pair;
+  const int pr = n_pairs - 1 - rem / P.n_kv_heads;
   I.g = rem % P.n_kv_heads;
-  I.tok_lo = qt * tok_per_tile;
-  I.tok_hi = min(q_len, I.tok_lo + tok_per_tile);
+  I.tok_lo = pr * tok_per_pair;
+  I.tok_hi = min(q_len, I.tok_lo + tok_per_pair);
   I.kv_hi = I.ctx + I.tok_hi;
   I.nkt = (I.kv_hi + kTileN - 1) / kTileN;
   return I;
@@ -83,6 +94,15 @@ __device__ __forceinline__ bool warp_wait(const StepParams& P, uint64_t* bar, ui
   return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait of a single thread; a timeout records the error and aborts the CTA.
+__device__ __forceinline__ bool lane_wait(const StepParams& P, MixedCtl& C, uint64_t* bar, uint32_t parity) {
+  if (mbar_wait(bar, parity)) return true;
+  set_error(P.err, CB_DEVERR_TIMEOUT);
+  C.abort = 1;
+  return false;
+}
+
+// ---------------------------------------------------------------- producer (warp 8)
 template <int A, int G>
 __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
                          const CUtensorMap* qmap, PrefillTiles<A>& T, MixedCtl& C, const int* pre) {
@@ -93,30 +113,32 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
   const int n_pre = pre[P.n_reqs];
   const int Hkv = P.n_kv_heads;
   const int rows_total = P.num_blocks * Hkv * kBlockSize;
-  uint32_t kv_it = 0, it = 0;
+  // lane -> (block b, half hf) among the 8 x H boxes of one key/value tile
+  const int my_b = (lane / H) & 7, my_hf = lane % H;
+  const bool issuer = lane < 8 * H;
+  uint32_t kt = 0, it = 0;
   for (int item = blockIdx.x; item < n_pre; item += gridDim.x, ++it) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, TOK);
+    const PreItem I = pre_item(P, pre, item, 2 * TOK);
     int ok = 1;
     if (lane == 0) {
-      ok = mbar_wait(&C.q_empty, (it & 1) ^ 1);
+      ok = lane_wait(P, C, &C.q_empty, (it & 1) ^ 1);
       if (ok) {
-        mbar_arrive_expect_tx(&C.q_full, H * PrefillTiles<A>::kHalfBytes);
+        mbar_arrive_expect_tx(&C.q_full, 2 * PrefillTiles<A>::kTileBytes);
 #pragma unroll
-        for (int hf = 0; hf < H; ++hf) tma_load_3d(&T.q[hf][0][0], qmap, hf * 64, I.g * G, I.q0 + I.tok_lo, &C.q_full);
+        for (int side = 0; side < 2; ++side)
+#pragma unroll
+          for (int hf = 0; hf < H; ++hf)
+            tma_load_3d(&T.q[side][hf][0][0], qmap, hf * 64, I.g * G, I.q0 + I.tok_lo + side * TOK, &C.q_full);
       }
     }
-    if (!__shfl_sync(FULL, ok, 0)) {
-      if (lane == 0) set_error(P.err, CB_DEVERR_TIMEOUT);
-      C.abort = 1;
-      break;
-    }
+    if (!__shfl_sync(FULL, ok, 0)) break;
     const int nblk_hi = (I.kv_hi + kBlockSize - 1) / kBlockSize;
     int y = rows_total;
-    for (int j = 0; j < I.nkt; ++j, ++kv_it) {
+    for (int j = 0; j < I.nkt; ++j, ++kt) {
       if ((j & 3) == 0) {          // table entries for this tile and the next three
         const int blk = j * 8 + lane;
-        y = rows_total;
+        y = rows_total;            // past the extent: TMA fills zeros
         if (blk < nblk_hi) {
           const int e = __ldg(P.block_tables + (size_t)I.r * P.max_blocks_per_seq + blk);
           if (e >= 0 && e < P.num_blocks)
@@ -125,228 +147,243 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
             set_error(P.err, CB_DEVERR_BADBLOCK);
         }
       }
-      const int st = kv_it & 1;
-      const uint32_t ph = (kv_it >> 1) & 1;
+      const int yb = __shfl_sync(FULL, y, (j & 3) * 8 + my_b);
+      const int st = kt & 1;
+      const uint32_t ph = (kt >> 1) & 1;
       ok = 1;
-      if (lane == 0) ok = mbar_wait(&C.kv_empty[st], ph ^ 1);
-      if (!__shfl_sync(FULL, ok, 0)) {
-        if (lane == 0) set_error(P.err, CB_DEVERR_TIMEOUT);
-        C.abort = 1;
-        break;
-      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&C.k_full[st], H * PrefillTiles<A>::kHalfBytes);
-        mbar_arrive_expect_tx(&C.v_full[st], H * PrefillTiles<A>::kHalfBytes);
+        ok = lane_wait(P, C, &C.k_empty[st], ph ^ 1);
+        if (ok) mbar_arrive_expect_tx(&C.k_full[st], PrefillTiles<A>::kTileBytes);
       }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int yb = __shfl_sync(FULL, y, (j & 3) * 8 + b);
-        if (lane == 0) {
-#pragma unroll
-          for (int hf = 0; hf < H; ++hf) {
-            tma_load_2d(&T.k[st][hf][b * kBlockSize][0], kmap, hf * 64, yb, &C.k_full[st]);
-            tma_load_2d(&T.v[st][hf][b * kBlockSize][0], vmap, hf * 64, yb, &C.v_full[st]);
-          }
-        }
+      if (!__shfl_sync(FULL, ok, 0)) break;
+      if (issuer) tma_load_2d(&T.k[st][my_hf][my_b * kBlockSize][0], kmap, my_hf * 64, yb, &C.k_full[st]);
+      if (lane == 0) {
+        ok = lane_wait(P, C, &C.v_empty[st], ph ^ 1);
+        if (ok) mbar_arrive_expect_tx(&C.v_full[st], PrefillTiles<A>::kTileBytes);
       }
+      if (!__shfl_sync(FULL, ok, 0)) break;
+      if (issuer) tma_load_2d(&T.v[st][my_hf][my_b * kBlockSize][0], vmap, my_hf * 64, yb, &C.v_full[st]);
     }
     if (C.abort) break;
   }
-  // drain: every load issued above has landed before shared memory is reused
-  if (lane == 0 && C.abort) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_wait(&C.k_full[s], 0, 20000000ull);
-      mbar_wait(&C.k_full[s], 1, 20000000ull);
-      mbar_wait(&C.v_full[s], 0, 20000000ull);
-      mbar_wait(&C.v_full[s], 1, 20000000ull);
-    }
+  if (lane == 0 && C.abort) {      // let copies already issued land before shared memory is reused
+    for (int s = 0; s < 2; ++s)
+      for (int par = 0; par < 2; ++par) {
+        mbar_wait(&C.k_full[s], par, 20000000ull);
+        mbar_wait(&C.v_full[s], par, 20000000ull);
+      }
     mbar_wait(&C.q_full, 0, 20000000ull);
     mbar_wait(&C.q_full, 1, 20000000ull);
   }
 }
 
-template <int A, int G>
-__device__ void mma_issuer(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C, const int* pre, uint32_t tmem) {
-  constexpr int TOK = kTileM / G;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, A, 1);
-  const int n_pre = pre[P.n_reqs];
-  const uint32_t q_s = smem_u32(&T.q[0][0][0]);
-  const uint32_t p_s = smem_u32(&T.p[0][0][0]);
-  const uint32_t tm_o = tmem + 256;
-  uint32_t kv_it = 0, it = 0;
-  bool ok = true;
-  auto issue_s = [&](uint32_t kvj) -> bool {
-    const int st = kvj & 1;
-    const uint32_t ph = (kvj >> 1) & 1;
-    if (!mbar_wait(&C.k_full[st], ph) || !mbar_wait(&C.s_free[st], ph ^ 1)) return false;
+// ---------------------------------------------------------------- MMA issuer (warp 9, one lane)
+template <int A>
+struct MmaIssuer {
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, A, 1);
+  const StepParams& P;
+  PrefillTiles<A>& T;
+  MixedCtl& C;
+  uint32_t tmem;
+  uint32_t pv_cnt0 = 0, pv_cnt1 = 0;   // O += P V issued per side (= o_done phases)
+  uint32_t p_cnt0 = 0, p_cnt1 = 0;     // P tiles consumed per side (= p_full phases)
+
+  __device__ MmaIssuer(const StepParams& p, PrefillTiles<A>& t, MixedCtl& c, uint32_t tm)
+      : P(p), T(t), C(c), tmem(tm) {}
+
+  // S_side = Q_side K(kj)^T into the side's S columns
+  template <int SIDE>
+  __device__ bool issue_s(uint32_t kj) {
+    const int st = kj & 1;
+    const uint32_t ph = (kj >> 1) & 1;
+    if (SIDE == 0 && !lane_wait(P, C, &C.k_full[st], ph)) return false;
+    // the previous O += P V of this side reads P from these columns: let it finish
+    const uint32_t pv = SIDE == 0 ? pv_cnt0 : pv_cnt1;
+    if (pv > 0 && !lane_wait(P, C, &C.o_done[SIDE], (pv - 1) & 1)) return false;
     tc_fence_after();
+    const uint32_t q_s = smem_u32(&T.q[SIDE][0][0][0]);
     const uint32_t k_s = smem_u32(&T.k[st][0][0][0]);
 #pragma unroll
     for (int ks = 0; ks < A / 16; ++ks) {
       const uint32_t off = (ks >> 2) * PrefillTiles<A>::kHalfBytes + (ks & 3) * 32;
-      tc_mma_f16(tmem + st * 128, smem_desc_sw128(q_s + off, 16, 1024), smem_desc_sw128(k_s + off, 16, 1024),
+      tc_mma_f16(tmem + SIDE * 128, smem_desc_sw128(q_s + off, 16, 1024), smem_desc_sw128(k_s + off, 16, 1024),
                  kIdescS, ks > 0);
     }
-    tc_commit(&C.s_full[st]);
+    tc_commit(&C.s_full[SIDE]);
+    if (SIDE == 1) tc_commit(&C.k_empty[st]);
     return true;
-  };
+  }
+
+  // O_side (+)= P_side V(kj), P read from tensor memory
+  template <int SIDE>
+  __device__ bool issue_pv(int j, uint32_t kj, uint32_t it) {
+    const int st = kj & 1;
+    const uint32_t ph = (kj >> 1) & 1;
+    uint32_t& pc = SIDE == 0 ? p_cnt0 : p_cnt1;
+    if (!lane_wait(P, C, &C.p_full[SIDE], pc & 1)) return false;
+    ++pc;
+    if (j == 0 && !lane_wait(P, C, &C.o_free[SIDE], (it & 1) ^ 1)) return false;
+    if (SIDE == 0 && !lane_wait(P, C, &C.v_full[st], ph)) return false;
+    tc_fence_after();
+    const uint32_t v_s = smem_u32(&T.v[st][0][0][0]);
+    const uint32_t p_t = tmem + SIDE * 128;
+    const uint32_t o_t = tmem + 256 + SIDE * A;
+#pragma unroll
+    for (int ks = 0; ks < kTileN / 16; ++ks)
+      tc_mma_f16_ts(o_t, p_t + ks * 8, smem_desc_sw128(v_s + ks * 16 * 128, PrefillTiles<A>::kHalfBytes, 1024),
+                    kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+    tc_commit(&C.o_done[SIDE]);
+    if (SIDE == 0)
+      ++pv_cnt0;
+    else
+      ++pv_cnt1;
+    if (SIDE == 1) tc_commit(&C.v_empty[st]);
+    return true;
+  }
+};
+
+template <int A, int G>
+__device__ void mma_issuer(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C, const int* pre, uint32_t tmem) {
+  constexpr int TOK = kTileM / G;
+  const int n_pre = pre[P.n_reqs];
+  MmaIssuer<A> M(P, T, C, tmem);
+  uint32_t kt = 0, it = 0;
+  bool ok = true;
   for (int item = blockIdx.x; item < n_pre && ok; item += gridDim.x, ++it) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, TOK);
-    if (!mbar_wait(&C.q_full, it & 1)) {
+    const PreItem I = pre_item(P, pre, item, 2 * TOK);
+    if (!lane_wait(P, C, &C.q_full, it & 1)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    if (!issue_s(kv_it)) {
+    if (!M.template issue_s<0>(kt) || !M.template issue_s<1>(kt)) {
       ok = false;
       break;
     }
-    for (int j = 0; j < I.nkt; ++j) {
-      const uint32_t kvj = kv_it + j;
-      if (j + 1 < I.nkt) {
-        if (!issue_s(kvj + 1)) {
-          ok = false;
-          break;
-        }
-      } else {
-        tc_commit(&C.q_empty);    // the last S of this item has been issued: Q free once it completes
-      }
-      const int st = kvj & 1;
-      const uint32_t ph = (kvj >> 1) & 1;
-      if (!mbar_wait(&C.p_full, kvj & 1) || (j == 0 && !mbar_wait(&C.o_free, (it & 1) ^ 1)) ||
-          !mbar_wait(&C.v_full[st], ph)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t v_s = smem_u32(&T.v[st][0][0][0]);
-#pragma unroll
-      for (int ks = 0; ks < kTileN / 16; ++ks) {
-        const uint32_t poff = (ks >> 2) * PrefillTiles<A>::kHalfBytes + (ks & 3) * 32;
-        tc_mma_f16(tm_o, smem_desc_sw128(p_s + poff, 16, 1024),
-                   smem_desc_sw128(v_s + ks * 16 * 128, PrefillTiles<A>::kHalfBytes, 1024), kIdescPV,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-      }
-      tc_commit(&C.o_done);
-      tc_commit(&C.kv_empty[st]);
+    for (int j = 0; j < I.nkt && ok; ++j) {
+      const uint32_t kj = kt + j;
+      ok = M.template issue_pv<0>(j, kj, it) && M.template issue_pv<1>(j, kj, it);
+      if (!ok) break;
+      if (j + 1 < I.nkt)
+        ok = M.template issue_s<0>(kj + 1) && M.template issue_s<1>(kj + 1);
+      else
+        tc_commit(&C.q_empty);   // every S of this item is issued: Q is free once they complete
     }
-    kv_it += I.nkt;
+    kt += I.nkt;
   }
-  if (!ok) {
-    set_error(P.err, CB_DEVERR_TIMEOUT);
-    C.abort = 1;
-  }
-  tc_commit(&C.drain);           // every MMA issued above is complete before TMEM is freed
+  if (!ok) C.abort = 1;
+  tc_commit(&C.drain);           // every MMA issued above completes before TMEM is freed
   mbar_wait(&C.drain, 0, 20000000ull);
 }
 
+// ---------------------------------------------------------------- softmax (warps 0-7)
 template <int A, int G>
-__device__ void softmax_warps(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C, const int* pre, uint32_t tmem) {
+__device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C, const int* pre, uint32_t tmem,
+                             int side) {
   constexpr int TOK = kTileM / G;
   constexpr int H = A / 64;
   const unsigned FULL = 0xffffffffu;
-  const int row = threadIdx.x;               // 0..127
-  const int warp = row >> 5;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int row = threadIdx.x & 127;
+  const int warp_q = (threadIdx.x >> 5) & 3;                // TMEM lane quarter of this warp
+  const uint32_t lane_base = (uint32_t)(warp_q * 32) << 16;
+  const uint32_t s_col = side * 128;
+  const uint32_t o_col = 256 + side * A;
   const int n_pre = pre[P.n_reqs];
   const int Hq = P.n_q_heads;
   const float sl2 = P.scale_log2;
-  uint32_t kv_it = 0, it = 0;
-  for (int item = blockIdx.x; item < n_pre; item += gridDim.x, ++it) {
+  uint32_t sc = 0;                                           // S tiles consumed (= global key tiles)
+  for (int item = blockIdx.x; item < n_pre; item += gridDim.x) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, TOK);
+    const PreItem I = pre_item(P, pre, item, 2 * TOK);
     const int tok_l = row / G, gq = row % G;
-    const int ti = I.tok_lo + tok_l;
+    const int ti = I.tok_lo + side * TOK + tok_l;
     const bool valid_row = ti < I.tok_hi;
-    const int pos = I.ctx + min(ti, I.tok_hi - 1);     // last key this row may see
-    float m = kNegInf, l = 0.f;
+    const int pos = I.ctx + min(ti, I.tok_hi - 1);            // last key this row may see
+    float m = kNegInf, l = 0.f;                               // m: running max, times scale*log2 e
     bool ok = true;
-    for (int j = 0; j < I.nkt; ++j) {
-      const uint32_t kvj = kv_it + j;
-      const int st = kvj & 1;
-      const uint32_t ph = (kvj >> 1) & 1;
-      if (!warp_wait(P, &C.s_full[st], ph)) {
+    for (int j = 0; j < I.nkt; ++j, ++sc) {
+      if (!warp_wait(P, &C.s_full[side], sc & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + st * 128 + c * 32, s[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&C.s_free[st]);
       const int key0 = j * kTileN;
-      float mt = kNegInf;
-      if (key0 + kTileN - 1 <= pos) {
+      const bool masked_tile = key0 + kTileN - 1 > pos;
+      // pass 1: row max over the visible keys (32 columns at a time, next load in flight)
+      float mt;
+      {
+        float sb[2][32];
+        float a[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+        tmem_ld32(tmem + lane_base + s_col, sb[0]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) tmem_ld32(tmem + lane_base + s_col + (c + 1) * 32, sb[(c + 1) & 1]);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            s[c][k] *= sl2;
-            mt = fmaxf(mt, s[c][k]);
+            const float v = (masked_tile && key0 + c * 32 + k > pos) ? kNegInf : sb[c & 1][k];
+            a[k & 3] = fmaxf(a[k & 3], v);
           }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            s[c][k] = (key0 + c * 32 + k <= pos) ? s[c][k] * sl2 : kNegInf;
-            mt = fmaxf(mt, s[c][k]);
-          }
+          if (c < 3) tmem_wait_ld();
+        }
+        mt = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) * sl2;
       }
       const float mn = fmaxf(m, mt);
       const bool need = mn > m + 8.f;
-      if (j > 0) {
-        if (!warp_wait(P, &C.o_done, (kvj - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
       float alpha = 1.f;
       if (need) {
         alpha = ex2(m - mn);
         m = mn;
       }
       if (j > 0 && __any_sync(FULL, need)) {
+        // rescale O: the previous O += P V of this side must be complete
+        if (!warp_wait(P, &C.o_done[side], (sc - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < A / 32; ++c) {
           float o[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+          tmem_ld32(tmem + lane_base + o_col + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] *= alpha;
-          tmem_st32(tmem + lane_base + 256 + c * 32, o);
+          tmem_st32(tmem + lane_base + o_col + c * 32, o);
         }
-        tmem_wait_st();
       }
-      float rs = 0.f;
+      // pass 2: p = 2^(s*scale*log2 e - m), packed to bf16 pairs over the S columns
+      // (32 columns at a time, the next chunk's load in flight)
+      const float nm = -m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        float sb[2][32];
+        tmem_ld32(tmem + lane_base + s_col, sb[0]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) tmem_ld32(tmem + lane_base + s_col + (c + 1) * 32, sb[(c + 1) & 1]);
+          uint32_t pk[16];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int c = h2 * 2 + (ch >> 2), k0 = (ch & 3) * 8;
-          float pv[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            pv[k] = ex2(s[c][k0 + k] - m);
-            rs += pv[k];
+          for (int k = 0; k < 16; ++k) {
+            const int e = 2 * k, key = key0 + c * 32 + e;
+            const float p0 = (masked_tile && key > pos) ? 0.f : ex2(fmaf(sb[c & 1][e], sl2, nm));
+            const float p1 = (masked_tile && key + 1 > pos) ? 0.f : ex2(fmaf(sb[c & 1][e + 1], sl2, nm));
+            rs[k & 3] += p0 + p1;
+            pk[k] = pack_bf16(p0, p1);
           }
-          uint4 w;
-          w.x = pack_bf16(pv[0], pv[1]);
-          w.y = pack_bf16(pv[2], pv[3]);
-          w.z = pack_bf16(pv[4], pv[5]);
-          w.w = pack_bf16(pv[6], pv[7]);
-          *reinterpret_cast<uint4*>(&T.p[h2][row][(ch ^ (row & 7)) << 4]) = w;
+          if (c < 3) tmem_wait_ld();     // the next chunk has landed before P overwrites columns
+          tmem_st16u(tmem + lane_base + s_col + c * 16, pk);
         }
-      l = l * alpha + rs;
-      // rows past the last key of this tile's request part of the final block hold
-      // whatever the cache had there: zero them so 0 * (non-finite) cannot reach O
-      if (key0 + kTileN > I.kv_hi && (I.kv_hi & (kBlockSize - 1))) {
-        if (!warp_wait(P, &C.v_full[st], ph)) {
+      }
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      // side A zeroes the value rows past the pair's last key in its final block
+      // (they hold whatever the cache had there, so 0 * non-finite cannot reach O)
+      if (side == 0 && key0 + kTileN > I.kv_hi && (I.kv_hi & (kBlockSize - 1))) {
+        const int st = sc & 1;
+        if (!warp_wait(P, &C.v_full[st], (sc >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -357,17 +394,17 @@ __device__ void softmax_warps(const StepParams& P, PrefillTiles<A>& T, MixedCtl&
           const int rr = r0 + idx / (H * 8), rest = idx % (H * 8);
           *reinterpret_cast<uint4*>(&T.v[st][rest >> 3][rr][(rest & 7) << 4]) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&C.p_full);
+      mbar_arrive(&C.p_full[side]);
     }
     if (!ok) {
       C.abort = 1;
       break;
     }
-    const uint32_t kvl = kv_it + I.nkt - 1;
-    if (!warp_wait(P, &C.o_done, kvl & 1)) {
+    if (!warp_wait(P, &C.o_done[side], (sc - 1) & 1)) {
       C.abort = 1;
       break;
     }
@@ -377,7 +414,7 @@ __device__ void softmax_warps(const StepParams& P, PrefillTiles<A>& T, MixedCtl&
 #pragma unroll 1
     for (int c = 0; c < A / 32; ++c) {
       float o[32];
-      tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+      tmem_ld32(tmem + lane_base + o_col + c * 32, o);
       tmem_wait_ld();
       if (valid_row) {
 #pragma unroll
@@ -392,8 +429,7 @@ __device__ void softmax_warps(const StepParams& P, PrefillTiles<A>& T, MixedCtl&
       }
     }
     tc_fence_before();
-    mbar_arrive(&C.o_free);
-    kv_it += I.nkt;
+    mbar_arrive(&C.o_free[side]);
   }
 }
 
@@ -403,7 +439,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                  const __grid_constant__ CUtensorMap qmap) {
   constexpr int TOK = kTileM / G;
   using WS = DecWarpSmem<A, G, kDecStages>;
-  static_assert(6 * sizeof(WS) <= sizeof(PrefillTiles<A>), "decode rings must fit in the tile region");
+  static_assert(kDecWarps * sizeof(WS) <= sizeof(PrefillTiles<A>), "decode rings must fit in the tile region");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillTiles<A>& T = *reinterpret_cast<PrefillTiles<A>*>(base);
@@ -418,14 +454,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     mbar_init(&C.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&C.k_full[s], 1);
+      mbar_init(&C.k_empty[s], 1);
       mbar_init(&C.v_full[s], 1);
-      mbar_init(&C.kv_empty[s], 1);
+      mbar_init(&C.v_empty[s], 1);
       mbar_init(&C.s_full[s], 1);
-      mbar_init(&C.s_free[s], 128);
+      mbar_init(&C.p_full[s], 128);
+      mbar_init(&C.o_done[s], 1);
+      mbar_init(&C.o_free[s], 128);
     }
-    mbar_init(&C.p_full, 128);
-    mbar_init(&C.o_done, 1);
-    mbar_init(&C.o_free, 128);
     mbar_init(&C.drain, 1);
     C.abort = 0;
     fence_mbar_init();
@@ -433,33 +469,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     prefetch_tmap(&vmap);
     prefetch_tmap(&qmap);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&C.tmem_base, 512);
     tmem_relinquish();
     tc_fence_before();
   }
-  build_plan(P, TOK, dec, spl, pre, C.scratch);     // ends with __syncthreads()
+  build_plan(P, 2 * TOK, dec, spl, pre, C.scratch);     // ends with __syncthreads()
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
 
   if (pre[P.n_reqs] > 0) {
-    if (warp == 4) {
+    if (warp == 8) {
       producer<A, G>(P, &kmap, &vmap, &qmap, T, C, pre);
-    } else if (warp == 5) {
+    } else if (warp == 9) {
       if (lane == 0) mma_issuer<A, G>(P, T, C, pre, tmem);
       __syncwarp();
     } else {
-      softmax_warps<A, G>(P, T, C, pre, tmem);
+      softmax_side<A, G>(P, T, C, pre, tmem, warp >> 2);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (C.abort) return;
-  decode_worker<A, G, kDecStages>(P, &kmap, &vmap, reinterpret_cast<WS*>(base)[warp], dec, spl);
+  if (C.abort || warp >= kDecWarps) return;
+  decode_worker<A, G, kDecStages, 2>(P, &kmap, &vmap, reinterpret_cast<WS*>(base)[warp], dec, spl);
 }
 
 template <int A, int G>
