@@ -167,6 +167,13 @@ const char* cb_strerror(int code);
  * aligned) with a plain streaming kernel: the HBM copy roofline probe. */
 int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream);
 
+/* Diagnostic: out[i] = 2^t[i] computed on the device by the polynomial that the
+ * prefill softmax uses for part of its probabilities (FMA pipe instead of the
+ * special-function unit).  t, out: device float arrays of n elements, n even.
+ * Relative error below 1e-4 for -125 <= t <= 127; inputs below -125 give 2^-125.
+ * Returns CB_OK, CB_EINVAL (odd n, null pointer) or CB_ECUDA. */
+int cb_exp2_poly(const float* t, float* out, int n, void* stream);
+
 /* Number of kernels the last successful cb_paged_attention / cb_kv_append call
  * enqueued (for launch accounting in benchmarks). */
 int cb_last_launch_count(void);

@@ -268,4 +268,11 @@ int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream) {
 
 int cb_last_launch_count(void) { return g_last_launches; }
 
+int cb_exp2_poly(const float* t, float* out, int n, void* stream) {
+  if (!t || !out || n < 0 || (n & 1)) return CB_EINVAL;
+  if (launch_exp2_poly(t, out, n, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CB_ECUDA;
+  g_last_launches = 1;
+  return CB_OK;
+}
+
 }  // extern "C"

@@ -66,5 +66,6 @@ cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CU
 cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const CUtensorMap& qmap, int head_dim, int group, int n_sms, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
+cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream);
 
 }  // namespace cb

@@ -29,9 +29,10 @@
 //                         uses the same reference max), finally writes O/l.
 //              warp 8     TMA producer: Q pair, K tiles and V tiles into
 //                         separate 2-stage rings; 16 lanes issue the boxes.
-//              warp 9     MMA issuer (one lane): per key tile
-//                         PV_A(j), PV_B(j), S_A(j+1), S_B(j+1)
-//                         so one tile's softmax overlaps the other tile's MMAs.
+//              warp 9     MMA issuer (one lane): polls both tiles' chains
+//                         S(j), PV(j), S(j+1), ... and issues whichever MMA
+//                         is ready, so one tile's softmax overlaps the other
+//                         tile's MMAs.
 // Every wait is bounded.
 #include "cb_decode_item.cuh"
 
@@ -43,6 +44,13 @@ constexpr int kSmemLimit = 232448;
 constexpr int kNumThreads = 320;
 constexpr int kDecWarps = 8;
 constexpr int kDecStages = 2;
+// Of every 16 pairs of scores, pairs kPolyFrom..15 take 2^x from the FMA-pipe
+// polynomial instead of the special-function unit.  16 = off: measured on the
+// long-context chunk, the special-function unit is not the limiter here (the
+// tensor core's cost per 128x128x16 MMA with both operands in shared memory,
+// ~107 cycles, sets the pace), and the polynomial's extra instructions cost
+// 8% (954 vs 875 TFLOP/s with 4 of 16 pairs).
+constexpr int kPolyFrom = 16;
 
 template <int A>
 struct PrefillTiles {
@@ -178,6 +186,13 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
 }
 
 // ---------------------------------------------------------------- MMA issuer (warp 9, one lane)
+// Each query tile is an independent chain  S(0) P(0) PV(0) S(1) P(1) PV(1) ...
+// S(j+1) overwrites the columns PV(j) reads P from; both are issued by this one
+// thread, and tcgen05.mma operations of one thread execute in issue order, so
+// S(j+1) may be queued right behind PV(j).  The issuer polls both chains and
+// issues whichever next MMA is ready, so the two tiles drift half a period
+// apart: while one tile's softmax runs, the tensor core works on the other
+// tile's MMAs.
 template <int A>
 struct MmaIssuer {
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);
@@ -188,57 +203,59 @@ struct MmaIssuer {
   uint32_t tmem;
   uint32_t pv_cnt0 = 0, pv_cnt1 = 0;   // O += P V issued per side (= o_done phases)
   uint32_t p_cnt0 = 0, p_cnt1 = 0;     // P tiles consumed per side (= p_full phases)
+  // Shared-memory descriptors of the tile bases, built once.  The start-address
+  // field is the low 14 bits (address >> 4), so a K step of an operand is an
+  // add of a compile-time constant: the issuing thread spends a few cycles per
+  // MMA instead of rebuilding 64-bit descriptors in a serial chain.
+  uint64_t qd[2], kd[2], vd[2];
 
   __device__ MmaIssuer(const StepParams& p, PrefillTiles<A>& t, MixedCtl& c, uint32_t tm)
-      : P(p), T(t), C(c), tmem(tm) {}
+      : P(p), T(t), C(c), tmem(tm) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      qd[i] = smem_desc_sw128(smem_u32(&T.q[i][0][0][0]), 16, 1024);
+      kd[i] = smem_desc_sw128(smem_u32(&T.k[i][0][0][0]), 16, 1024);
+      vd[i] = smem_desc_sw128(smem_u32(&T.v[i][0][0][0]), PrefillTiles<A>::kHalfBytes, 1024);
+    }
+  }
 
-  // S_side = Q_side K(kj)^T into the side's S columns
+  // S_side = Q_side K(kj)^T, if its inputs are ready
   template <int SIDE>
-  __device__ bool issue_s(uint32_t kj) {
+  __device__ bool try_s(uint32_t kj) {
     const int st = kj & 1;
-    const uint32_t ph = (kj >> 1) & 1;
-    if (SIDE == 0 && !lane_wait(P, C, &C.k_full[st], ph)) return false;
-    // the previous O += P V of this side reads P from these columns: let it finish
-    const uint32_t pv = SIDE == 0 ? pv_cnt0 : pv_cnt1;
-    if (pv > 0 && !lane_wait(P, C, &C.o_done[SIDE], (pv - 1) & 1)) return false;
+    if (!mbar_ready(&C.k_full[st], (kj >> 1) & 1)) return false;
     tc_fence_after();
-    const uint32_t q_s = smem_u32(&T.q[SIDE][0][0][0]);
-    const uint32_t k_s = smem_u32(&T.k[st][0][0][0]);
+    const uint64_t q0 = qd[SIDE], k0 = kd[st];
 #pragma unroll
     for (int ks = 0; ks < A / 16; ++ks) {
-      const uint32_t off = (ks >> 2) * PrefillTiles<A>::kHalfBytes + (ks & 3) * 32;
-      tc_mma_f16(tmem + SIDE * 128, smem_desc_sw128(q_s + off, 16, 1024), smem_desc_sw128(k_s + off, 16, 1024),
-                 kIdescS, ks > 0);
+      const uint64_t off = ((ks >> 2) * PrefillTiles<A>::kHalfBytes + (ks & 3) * 32) >> 4;
+      tc_mma_f16(tmem + SIDE * 128, q0 + off, k0 + off, kIdescS, ks > 0);
     }
     tc_commit(&C.s_full[SIDE]);
-    if (SIDE == 1) tc_commit(&C.k_empty[st]);
     return true;
   }
 
-  // O_side (+)= P_side V(kj), P read from tensor memory
+  // O_side (+)= P_side V(kj) with P read from tensor memory, if ready
   template <int SIDE>
-  __device__ bool issue_pv(int j, uint32_t kj, uint32_t it) {
+  __device__ bool try_pv(int j, uint32_t kj, uint32_t it) {
     const int st = kj & 1;
-    const uint32_t ph = (kj >> 1) & 1;
     uint32_t& pc = SIDE == 0 ? p_cnt0 : p_cnt1;
-    if (!lane_wait(P, C, &C.p_full[SIDE], pc & 1)) return false;
+    if (!mbar_ready(&C.p_full[SIDE], pc & 1)) return false;
+    if (!mbar_ready(&C.v_full[st], (kj >> 1) & 1)) return false;
+    if (j == 0 && !mbar_ready(&C.o_free[SIDE], (it & 1) ^ 1)) return false;
     ++pc;
-    if (j == 0 && !lane_wait(P, C, &C.o_free[SIDE], (it & 1) ^ 1)) return false;
-    if (SIDE == 0 && !lane_wait(P, C, &C.v_full[st], ph)) return false;
     tc_fence_after();
-    const uint32_t v_s = smem_u32(&T.v[st][0][0][0]);
+    const uint64_t v0 = vd[st];
     const uint32_t p_t = tmem + SIDE * 128;
     const uint32_t o_t = tmem + 256 + SIDE * A;
 #pragma unroll
     for (int ks = 0; ks < kTileN / 16; ++ks)
-      tc_mma_f16_ts(o_t, p_t + ks * 8, smem_desc_sw128(v_s + ks * 16 * 128, PrefillTiles<A>::kHalfBytes, 1024),
-                    kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+      tc_mma_f16_ts(o_t, p_t + ks * 8, v0 + ((ks * 16 * 128) >> 4), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
     tc_commit(&C.o_done[SIDE]);
     if (SIDE == 0)
       ++pv_cnt0;
     else
       ++pv_cnt1;
-    if (SIDE == 1) tc_commit(&C.v_empty[st]);
     return true;
   }
 };
@@ -258,20 +275,53 @@ __device__ void mma_issuer(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C,
       break;
     }
     tc_fence_after();
-    if (!M.template issue_s<0>(kt) || !M.template issue_s<1>(kt)) {
-      ok = false;
-      break;
-    }
-    for (int j = 0; j < I.nkt && ok; ++j) {
-      const uint32_t kj = kt + j;
-      ok = M.template issue_pv<0>(j, kj, it) && M.template issue_pv<1>(j, kj, it);
-      if (!ok) break;
-      if (j + 1 < I.nkt)
-        ok = M.template issue_s<0>(kj + 1) && M.template issue_s<1>(kj + 1);
-      else
+    const int n = I.nkt;
+    int ns0 = 0, ns1 = 0, np0 = 0, np1 = 0;     // next S / next PV per side
+    bool q_released = false;
+    uint64_t t_last = globaltimer_ns();
+    while (np0 < n || np1 < n) {
+      bool prog = false;
+      // side A: its next S, or its next PV followed at once by the S after it,
+      // so this tile's scores never queue behind the other tile's MMAs
+      if (np0 < ns0 && M.template try_pv<0>(np0, kt + np0, it)) {
+        ++np0;
+        if (np1 >= np0) tc_commit(&C.v_empty[(kt + np0 - 1) & 1]);      // both sides read V(np0-1)
+        prog = true;
+      }
+      if (ns0 == np0 && ns0 < n && M.template try_s<0>(kt + ns0)) {
+        ++ns0;
+        if (ns1 >= ns0) tc_commit(&C.k_empty[(kt + ns0 - 1) & 1]);      // both sides read K(ns0-1)
+        prog = true;
+      }
+      // side B, the same
+      if (np1 < ns1 && M.template try_pv<1>(np1, kt + np1, it)) {
+        ++np1;
+        if (np0 >= np1) tc_commit(&C.v_empty[(kt + np1 - 1) & 1]);
+        prog = true;
+      }
+      if (ns1 == np1 && ns1 < n && M.template try_s<1>(kt + ns1)) {
+        ++ns1;
+        if (ns0 >= ns1) tc_commit(&C.k_empty[(kt + ns1 - 1) & 1]);
+        prog = true;
+      }
+      if (!q_released && ns0 == n && ns1 == n) {
         tc_commit(&C.q_empty);   // every S of this item is issued: Q is free once they complete
+        q_released = true;
+      }
+      if (prog) {
+        t_last = globaltimer_ns();
+      } else {
+        // nothing ready: yield the issue slot to the softmax warps of this
+        // sub-partition instead of spinning
+        __nanosleep(64);
+        if (globaltimer_ns() - t_last > kWaitLimitNs || C.abort) {
+          set_error(P.err, CB_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
     }
-    kt += I.nkt;
+    kt += n;
   }
   if (!ok) C.abort = 1;
   tc_commit(&C.drain);           // every MMA issued above completes before TMEM is freed
@@ -311,24 +361,27 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
       tc_fence_after();
       const int key0 = j * kTileN;
       const bool masked_tile = key0 + kTileN - 1 > pos;
-      // pass 1: row max over the visible keys (32 columns at a time, next load in flight)
+      // pass 1: row max over the visible keys (two 64-column loads)
       float mt;
       {
-        float sb[2][32];
         float a[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-        tmem_ld32(tmem + lane_base + s_col, sb[0]);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < 3) tmem_ld32(tmem + lane_base + s_col + (c + 1) * 32, sb[(c + 1) & 1]);
+        for (int h = 0; h < 2; ++h) {
+          float sv[64];
+          tmem_ld64(tmem + lane_base + s_col + h * 64, sv);
+          tmem_wait_ld();
+          if (!masked_tile) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float v = (masked_tile && key0 + c * 32 + k > pos) ? kNegInf : sb[c & 1][k];
-            a[k & 3] = fmaxf(a[k & 3], v);
+            for (int k = 0; k < 64; k += 2) a[(k >> 1) & 3] = max3(a[(k >> 1) & 3], sv[k], sv[k + 1]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              const int key = key0 + h * 64 + k;
+              a[(k >> 1) & 3] = max3(a[(k >> 1) & 3], key > pos ? kNegInf : sv[k], key + 1 > pos ? kNegInf : sv[k + 1]);
+            }
           }
-          if (c < 3) tmem_wait_ld();
         }
-        mt = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) * sl2;
+        mt = max3(a[0], a[1], fmaxf(a[2], a[3])) * sl2;
       }
       const float mn = fmaxf(m, mt);
       const bool need = mn > m + 8.f;
@@ -355,33 +408,48 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
         }
       }
       // pass 2: p = 2^(s*scale*log2 e - m), packed to bf16 pairs over the S columns
-      // (32 columns at a time, the next chunk's load in flight)
-      const float nm = -m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        float sb[2][32];
-        tmem_ld32(tmem + lane_base + s_col, sb[0]);
+      // (64 columns per load).  Pairs are computed with packed fp32x2 FMA; pairs
+      // kPolyFrom..15 of every 16 take 2^x from the FMA-pipe polynomial to
+      // offload the special-function unit.
+      const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
+      uint64_t rs2[2] = {0ull, 0ull};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float sv[64];
+        tmem_ld64(tmem + lane_base + s_col + h * 64, sv);
         tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < 3) tmem_ld32(tmem + lane_base + s_col + (c + 1) * 32, sb[(c + 1) & 1]);
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int e = 2 * k, key = key0 + c * 32 + e;
-            const float p0 = (masked_tile && key > pos) ? 0.f : ex2(fmaf(sb[c & 1][e], sl2, nm));
-            const float p1 = (masked_tile && key + 1 > pos) ? 0.f : ex2(fmaf(sb[c & 1][e + 1], sl2, nm));
-            rs[k & 3] += p0 + p1;
-            pk[k] = pack_bf16(p0, p1);
+        for (int k = 0; k < 32; ++k) {
+          const uint64_t t = ffma2(f2(sv[2 * k], sv[2 * k + 1]), sl2x2, nmx2);
+          float p0, p1;
+          if ((k & 15) >= kPolyFrom) {
+            exp2_poly_pair(t, p0, p1);
+          } else {
+            float t0, t1;
+            f2split(t, t0, t1);
+            p0 = ex2(t0);
+            p1 = ex2(t1);
           }
-          if (c < 3) tmem_wait_ld();     // the next chunk has landed before P overwrites columns
-          tmem_st16u(tmem + lane_base + s_col + c * 16, pk);
+          if (masked_tile) {
+            const int key = key0 + h * 64 + 2 * k;
+            p0 = key > pos ? 0.f : p0;
+            p1 = key + 1 > pos ? 0.f : p1;
+          }
+          rs2[k & 1] = fadd2(rs2[k & 1], f2(p0, p1));
+          pk[k] = pack_bf16(p0, p1);
         }
+        // P of columns [64h, 64h+64) goes to columns [32h, 32h+32): S there was read above
+        tmem_st32u(tmem + lane_base + s_col + h * 32, pk);
       }
+      float rs[4];
+      f2split(rs2[0], rs[0], rs[1]);
+      f2split(rs2[1], rs[2], rs[3]);
       l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      // side A zeroes the value rows past the pair's last key in its final block
-      // (they hold whatever the cache had there, so 0 * non-finite cannot reach O)
-      if (side == 0 && key0 + kTileN > I.kv_hi && (I.kv_hi & (kBlockSize - 1))) {
+      // zero the value rows past the pair's last key in its final block: they hold
+      // whatever the cache had there, and 0 * non-finite must not reach O.  Both
+      // sides write the same zeros, since either side's O += P V may run first.
+      if (key0 + kTileN > I.kv_hi && (I.kv_hi & (kBlockSize - 1))) {
         const int st = sc & 1;
         if (!warp_wait(P, &C.v_full[st], (sc >> 1) & 1)) {
           ok = false;
