@@ -10,13 +10,18 @@ namespace {
 
 constexpr int kSmemLimit = 232448;   // opt-in dynamic shared memory per CTA on this part
 
+// Shape (measured best among 7-10 warps x 2-3 stages): NST ring stages per
+// warp, as many warps (<= 10) as shared memory holds, QK loop unrolled by 2
+// (enough ILP, and registers for 10 warps).  An L2 prefetch of blocks beyond
+// the ring was tried and only added traffic.
 template <int A, int G>
 struct DecodeCfg {
-  static constexpr int NST = A == 128 ? 3 : 4;
+  static constexpr int NST = A == 128 ? 2 : 4;
+  static constexpr int QKU = 2;
   using WS = DecWarpSmem<A, G, NST>;
   static constexpr int kPlanMax = (2 * (kMaxReqs + 1) + 96) * 4;
   static constexpr int NW_fit = (kSmemLimit - 1024 - kPlanMax) / (int)sizeof(WS);
-  static constexpr int NW = NW_fit < 8 ? NW_fit : 8;
+  static constexpr int NW = NW_fit < 10 ? NW_fit : 10;
   static_assert(NW >= 4, "decode ring does not fit");
 };
 
@@ -36,7 +41,7 @@ __global__ void __launch_bounds__(DecodeCfg<A, G>::NW * 32, 1)
     prefetch_tmap(&vmap);
   }
   build_plan(P, 1, dec, spl, nullptr, scratch);
-  decode_worker<A, G, C::NST>(P, &kmap, &vmap, rings[threadIdx.x >> 5], dec, spl);
+  decode_worker<A, G, C::NST, C::QKU>(P, &kmap, &vmap, rings[threadIdx.x >> 5], dec, spl);
 }
 
 template <int A, int G>

@@ -211,13 +211,14 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
   const int npro = min(NST, nb);
   for (int i = 0; i < npro; ++i) issue(i, i);
 
-  float m[G], lsum[G], acc[G][DPL];
+  float m[G], lsum[G];
+  uint64_t acc2[G][DPL / 2];     // unnormalised output columns (d0, d0+1), (d0+2, d0+3) as fp32 pairs
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     m[j] = kNegInf;
     lsum[j] = 0.f;
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[j][k] = 0.f;
+    for (int k = 0; k < DPL / 2; ++k) acc2[j][k] = 0ull;
   }
   const int tq = lane & 15, hf_l = lane >> 4;
   const int d0 = lane * DPL;
@@ -232,32 +233,38 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
     }
     parity ^= 1u << st;
     const int tokbase = (b0 + i) * kBlockSize;
-    // ---- QK for token tq over half hf_l of head_dim
+    // ---- QK for token tq over half hf_l of head_dim: packed fp32x2 FMAs on
+    // (even, odd) column pairs, two accumulators per head
     float s[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) s[j] = 0.f;
     {
-      float part[G][2];
+      uint64_t part[G][2];
 #pragma unroll
-      for (int j = 0; j < G; ++j) part[j][0] = part[j][1] = 0.f;
+      for (int j = 0; j < G; ++j) part[j][0] = part[j][1] = 0ull;
 #pragma unroll QKU
       for (int ci = 0; ci < CPL; ++ci) {
         const int cc = hf_l * CPL + ci;        // logical 16-byte chunk of the row
         const int half = cc >> 3, pos = cc & 7;
         const uint4 kw =
             *reinterpret_cast<const uint4*>(&S.kv[st][0][half][tq][(pos ^ (tq & 7)) << 4]);
-        const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                             bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
+        const uint64_t k01 = f2(bf16lo(kw.x), bf16hi(kw.x)), k23 = f2(bf16lo(kw.y), bf16hi(kw.y));
+        const uint64_t k45 = f2(bf16lo(kw.z), bf16hi(kw.z)), k67 = f2(bf16lo(kw.w), bf16hi(kw.w));
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-          const float4 qa = *reinterpret_cast<const float4*>(&S.q[j][cc * 8]);
-          const float4 qb = *reinterpret_cast<const float4*>(&S.q[j][cc * 8 + 4]);
-          part[j][ci & 1] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3];
-          part[j][ci & 1] += qb.x * kf[4] + qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(&S.q[j][cc * 8]);
+          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(&S.q[j][cc * 8 + 4]);
+          part[j][0] = ffma2(qa.x, k01, part[j][0]);
+          part[j][1] = ffma2(qa.y, k23, part[j][1]);
+          part[j][0] = ffma2(qb.x, k45, part[j][0]);
+          part[j][1] = ffma2(qb.y, k67, part[j][1]);
         }
       }
 #pragma unroll
-      for (int j = 0; j < G; ++j) s[j] = part[j][0] + part[j][1];
+      for (int j = 0; j < G; ++j) {
+        float a, b, c, d;
+        f2split(part[j][0], a, b);
+        f2split(part[j][1], c, d);
+        s[j] = (a + b) + (c + d);
+      }
     }
     const bool tvalid = tokbase + tq < kv;
 #pragma unroll
@@ -277,17 +284,21 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
       const float alpha = ex2(m[j] - mn);
       const float pj = ex2(s[j] - mn);
       lsum[j] = lsum[j] * alpha + (hf_l == 0 ? pj : 0.f);
+      const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) acc[j][k] *= alpha;
+      for (int k = 0; k < DPL / 2; ++k) acc2[j][k] = fmul2(acc2[j][k], a2);
       m[j] = mn;
       if (hf_l == 0) S.p[tq][j] = pj;
     }
     __syncwarp();
-    // ---- PV: this lane's DPL dims
+    // ---- PV: this lane's DPL dims.  Always 16 unrolled token steps (the loads
+    // of all steps can be in flight together); a token past the request's last
+    // key contributes exactly zero (its V is replaced by 0, its p is already 0).
     {
       const int cc = d0 >> 3, half = cc >> 3, pos = cc & 7, boff = (d0 & 7) * 2;
-      const int tend = min(kBlockSize, kv - tokbase);
-      for (int tt = 0; tt < tend; ++tt) {
+      const int nvalid = kv - tokbase;
+#pragma unroll
+      for (int tt = 0; tt < kBlockSize; ++tt) {
         const uint8_t* vrow = &S.kv[st][1][half][tt][((pos ^ (tt & 7)) << 4) + boff];
         float vf[DPL];
         if constexpr (DPL == 4) {
@@ -301,11 +312,32 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
           vf[0] = bf16lo(w);
           vf[1] = bf16hi(w);
         }
+        if (tt >= nvalid) {
+#pragma unroll
+          for (int k = 0; k < DPL; ++k) vf[k] = 0.f;
+        }
+        float pj[G];
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int j = 0; j < G; j += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(&S.p[tt][j]);
+            pj[j] = p4.x;
+            pj[j + 1] = p4.y;
+            pj[j + 2] = p4.z;
+            pj[j + 3] = p4.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < G; ++j) pj[j] = S.p[tt][j];
+        }
+        const uint64_t v01 = f2(vf[0], vf[1]);
+        uint64_t v23 = 0ull;
+        if constexpr (DPL == 4) v23 = f2(vf[2], vf[3]);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-          const float pj = S.p[tt][j];
-#pragma unroll
-          for (int k = 0; k < DPL; ++k) acc[j][k] += pj * vf[k];
+          const uint64_t pp = f2(pj[j], pj[j]);
+          acc2[j][0] = ffma2(pp, v01, acc2[j][0]);
+          if constexpr (DPL == 4) acc2[j][1] = ffma2(pp, v23, acc2[j][1]);
         }
       }
     }
@@ -323,6 +355,11 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
   }
 
   // ---- totals and output
+  float acc[G][DPL];
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int k = 0; k < DPL / 2; ++k) f2split(acc2[j][k], acc[j][2 * k], acc[j][2 * k + 1]);
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     float l = lsum[j];
