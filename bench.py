@@ -448,13 +448,194 @@ def run_ours(args, shape, desc, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- continuous-batching trace
+TRACE_DESC = ("trace: 256 requests, prompts min(8192, lognormal(ln 512, 1)), outputs geometric mean 256, "
+              "Poisson 2/step, FCFS budget 2048, 32 layers GQA 32/8 x128 bf16, block 16, 60 GB pool")
+
+
+def run_trace(args, world, rank, local):
+    """Continuous batching end to end: every iteration the host scheduler
+    (cb_sched_step) picks the batch and builds its metadata, which is copied
+    to the device; then, for each layer, the new rows are appended and the
+    paged attention runs.  New K/V/Q rows are per-layer seeded random buffers
+    (no projections), reused every iteration."""
+    import torch
+    from paged_kv_cache_cb_gb300 import _lib as L
+    if not os.path.exists(L.LIB_PATH):
+        from paged_kv_cache_cb_gb300 import build
+        build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    tr = wl.trace(seed=args.seed + rank, pool_bytes=int(args.trace_pool_gb * wl.GB), n_layers=args.trace_layers)
+    nl, hq, hk, a, bs, budget = tr.n_layers, tr.n_q_heads, tr.n_kv_heads, tr.head_dim, tr.block_size, tr.token_budget
+    nb = tr.num_blocks
+    bf = torch.bfloat16
+    kc = [torch.empty((nb, hk, bs, a), dtype=bf, device=dev) for _ in range(nl)]
+    vc = [torch.empty((nb, hk, bs, a), dtype=bf, device=dev) for _ in range(nl)]
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed + 17)
+    qn = [torch.randn((budget, hq, a), generator=g, device=dev, dtype=bf) for _ in range(nl)]
+    kn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=bf) for _ in range(nl)]
+    vn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=bf) for _ in range(nl)]
+    out = torch.empty((budget, hq, a), dtype=bf, device=dev)
+    maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
+    max_seq = max(p + o - 1 for _, p, o in tr.requests)
+    sched = L.Scheduler(nb, bs, budget, min(budget, L.CB_MAX_REQS), wl.free_order(nb, tr.seed), maxblk)
+    for arr, p, o in tr.requests:
+        sched.add_request(arr, p, o)
+    ws = torch.empty(L.cb_paged_attention_workspace_size(min(budget, L.CB_MAX_REQS), budget, budget, max_seq, hq, hk,
+                                                         a, bs), dtype=torch.uint8, device=dev)
+    d_cu = torch.zeros(budget + 1, dtype=torch.int32, device=dev)
+    d_ctx = torch.zeros(budget, dtype=torch.int32, device=dev)
+    d_bt = torch.zeros((budget, maxblk), dtype=torch.int32, device=dev)
+    d_sl = torch.zeros(budget, dtype=torch.int64, device=dev)
+    # double-buffered pinned staging of the metadata
+    h = [dict(cu=torch.zeros(budget + 1, dtype=torch.int32).pin_memory(),
+              ctx=torch.zeros(budget, dtype=torch.int32).pin_memory(),
+              bt=torch.zeros((budget, maxblk), dtype=torch.int32).pin_memory(),
+              sl=torch.zeros(budget, dtype=torch.int64).pin_memory(),
+              ev=torch.cuda.Event()) for _ in range(2)]
+    scale = 1.0 / math.sqrt(a)
+    stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0)
+
+    def one_step(i, host_io=None):
+        m = sched.step()
+        b, t = len(m["req_ids"]), int(m["cu_q_lens"][-1]) if len(m["req_ids"]) else 0
+        stats["preempted"] += m["n_preempted"]
+        if t == 0:
+            stats["idle"] += 1
+            return
+        hb = h[i & 1]
+        hb["ev"].synchronize()                    # this staging buffer's previous copy has finished
+        hb["cu"].numpy()[:b + 1] = m["cu_q_lens"]
+        hb["ctx"].numpy()[:b] = m["ctx_lens"]
+        hb["bt"].numpy()[:b] = m["block_tables"]
+        hb["sl"].numpy()[:t] = m["slot_mapping"]
+        d_cu[:b + 1].copy_(hb["cu"][:b + 1], non_blocking=True)
+        d_ctx[:b].copy_(hb["ctx"][:b], non_blocking=True)
+        d_bt[:b].copy_(hb["bt"][:b], non_blocking=True)
+        d_sl[:t].copy_(hb["sl"][:t], non_blocking=True)
+        hb["ev"].record(stream)
+        q_lens, ctx = m["q_lens"], m["ctx_lens"]
+        max_q, max_kv = int(q_lens.max()), int((q_lens + ctx).max())
+        for layer in range(nl):
+            if host_io is not None:                 # end-to-end: this step's rows come from pinned host memory
+                qn[layer][:t].copy_(host_io["q"][layer][:t], non_blocking=True)
+                kn[layer][:t].copy_(host_io["k"][layer][:t], non_blocking=True)
+                vn[layer][:t].copy_(host_io["v"][layer][:t], non_blocking=True)
+            L.cb_kv_append(kn[layer][:t], vn[layer][:t], d_sl[:t], kc[layer], vc[layer], stream)
+            stats["launches"] += L.cb_last_launch_count()
+            L.cb_paged_attention(qn[layer][:t], d_cu[:b + 1], d_ctx[:b], d_bt[:b], kc[layer], vc[layer], out[:t], scale,
+                                 ws, max_q, max_kv, stream)
+            stats["launches"] += L.cb_last_launch_count()
+            if host_io is not None:
+                host_io["out"][:t].copy_(out[:t], non_blocking=True)
+        stats["tokens"] += t
+        stats["steps"] += 1
+        dec = int((q_lens == 1).sum())
+        stats["dec"] += dec
+        stats["pre"] += t - dec
+        kvl = (q_lens + ctx).astype(np.int64)
+        stats["kv_bytes"] += int(2 * kvl.sum() * hk * a * 2) * nl
+        pairs = (q_lens.astype(np.int64) * ctx + q_lens.astype(np.int64) * (q_lens + 1) // 2).sum()
+        stats["flops"] += int(4 * a * hq * pairs) * nl
+        if host_io is not None:
+            stream.synchronize()
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+    if L.cb_last_error(stream) != 0:
+        raise RuntimeError("trace warm-up failed")
+    for k in list(stats):
+        stats[k] = 0
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    i = 0
+    while i < args.steps and not sched.done():
+        one_step(args.warmup + i)
+        i += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    status = L.cb_last_error(stream)
+    if status != 0:
+        raise RuntimeError("trace failed: " + L.cb_strerror(status))
+    dev_s = e0.elapsed_time(e1) * 1e-3
+    timed = dict(stats)
+    elapsed = max_over_ranks(wall, world, dev)
+    # end to end: the following iterations take their new rows from pinned host
+    # memory and return every layer's output to the host
+    e2e = None
+    if not sched.done():
+        host_io = dict(q=[t.cpu().pin_memory() for t in qn], k=[t.cpu().pin_memory() for t in kn],
+                       v=[t.cpu().pin_memory() for t in vn], out=torch.empty_like(out, device="cpu").pin_memory())
+        for k in list(stats):
+            stats[k] = 0
+        n_e2e = min(50, args.steps)
+        te = time.perf_counter()
+        j = 0
+        while j < n_e2e and not sched.done():
+            one_step(args.warmup + args.steps + j, host_io)
+            j += 1
+        te = max_over_ranks(time.perf_counter() - te, world, dev)
+        t_e = stats["tokens"]
+        e2e = {"value": t_e * world / te if te > 0 else None, "unit": UNIT,
+               "h2d_bytes_per_step": int(nl * (budget * (hq + 2 * hk) * a * 2)) if j else 0,
+               "d2h_bytes_per_step": int(nl * budget * hq * a * 2) if j else 0, "steps": j,
+               "note": "h2d/d2h per step counted at the full 2048-token budget (upper bound)"}
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    t_hbm = timed["kv_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = timed["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = timed["kv_bytes"] / dev_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": None, "kernel": "whole iteration (32 x append + attention), device time",
+                "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        ach = timed["flops"] / dev_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "kernel": "whole iteration (32 x append + attention), device time",
+                "peak_source": peaks["source"] + " bf16_tflops_sustained"}
+    line = {
+        "metric": METRIC, "value": timed["tokens"] * world / elapsed, "unit": UNIT, "n_gpus": world,
+        "steps": timed["steps"], "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(1, timed["steps"]),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": TRACE_DESC, "n_layers": nl, "num_blocks": nb, "token_budget": budget,
+                   "decode_tokens": timed["dec"], "prefill_tokens": timed["pre"], "idle_steps": timed["idle"],
+                   "preemptions": timed["preempted"],
+                   "l2": "inputs larger than L2: each iteration reads every running request's K/V in 32 layers",
+                   "parallelism": f"replicas x{world} (independent traces, no collective)"},
+        "roofline": roof, "device_s": dev_s, "wall_s": wall,
+        "cpu_baseline": None, "e2e": e2e, "gpu_launches": timed["launches"], "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + ["trace"])
+    ap.add_argument("--trace-pool-gb", type=float, default=60.0, help="trace: K+V pool of all layers")
+    ap.add_argument("--trace-layers", type=int, default=32, help="trace: attention layers per iteration")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", action="store_true", help="skip the in-process HBM copy probe")
@@ -462,6 +643,15 @@ def main(argv=None):
                     help="K+V block pool size (blocks stay randomly scattered over it)")
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
+    if args.workload == "trace":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "trace workload: the reference arm times single steps"}))
+            return
+        run_trace(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     make, desc = WORKLOADS[args.workload]
     if args.pool_gb != 20.0:
         desc = desc.replace("20 GB pool", f"{args.pool_gb:g} GB pool") + f" (pool {args.pool_gb:g} GB)"

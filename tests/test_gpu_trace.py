@@ -1,0 +1,82 @@
+"""Continuous batching end to end on the GPU: the C++ FCFS scheduler picks each
+iteration's batch (chunked prefills, decodes, preemption by recompute on a
+tight block pool), the library appends the new rows through the scheduler's slot
+mapping and runs attention through its block tables.  A host shadow records
+every (layer, request, position) row written; the fp64 oracle, fed from that
+shadow in the pages' contiguous layout, must agree with the GPU outputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import L, assert_close
+from oracle import attention as oa
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(rng, shape):
+    return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("seed,num_blocks", [(1, 16), (2, 20)])
+def test_scheduled_trace_matches_oracle(seed, num_blocks):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = L()
+    tr = wl.small_trace(seed, num_blocks=num_blocks)
+    hq, hk, a, bs, nl = 8, 2, 64, tr.block_size, 2
+    maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
+    max_seq = max(p + o - 1 for _, p, o in tr.requests)
+    sched = lib.Scheduler(tr.num_blocks, bs, tr.token_budget, tr.token_budget, wl.free_order(tr.num_blocks, tr.seed),
+                          maxblk)
+    for arr, p, o in tr.requests:
+        sched.add_request(arr, p, o)
+    kc = [torch.zeros(tr.num_blocks, hk, bs, a, dtype=torch.bfloat16, device="cuda") for _ in range(nl)]
+    vc = [torch.zeros_like(kc[0]) for _ in range(nl)]
+    ws = torch.empty(lib.cb_paged_attention_workspace_size(tr.token_budget, tr.token_budget, tr.token_budget, max_seq,
+                                                           hq, hk, a, bs), dtype=torch.uint8, device="cuda")
+    shadow = [dict() for _ in range(nl)]          # (rid, pos) -> (k row, v row), float64
+    rng = np.random.default_rng(seed)
+    steps = checked = preempted = 0
+    while not sched.done() and steps < 2000:
+        m = sched.step()
+        steps += 1
+        preempted += m["n_preempted"]
+        b = len(m["req_ids"])
+        if b == 0:
+            continue
+        t = int(m["cu_q_lens"][-1])
+        cu = torch.from_numpy(m["cu_q_lens"]).cuda()
+        ctx = torch.from_numpy(m["ctx_lens"]).cuda()
+        bt = torch.from_numpy(np.ascontiguousarray(m["block_tables"])).cuda()
+        sl = torch.from_numpy(m["slot_mapping"]).cuda()
+        q_lens, ctx_lens = m["q_lens"].tolist(), m["ctx_lens"].tolist()
+        check = steps % 3 == 0 or m["n_preempted"] > 0
+        for layer in range(nl):
+            q, k, v = _bf16(rng, (t, hq, a)), _bf16(rng, (t, hk, a)), _bf16(rng, (t, hk, a))
+            lib.cb_kv_append(k.cuda(), v.cuda(), sl, kc[layer], vc[layer])
+            out = torch.empty(t, hq, a, dtype=torch.bfloat16, device="cuda")
+            lib.cb_paged_attention(q.cuda(), cu, ctx, bt, kc[layer], vc[layer], out, 1 / math.sqrt(a), ws,
+                                   max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens)))
+            kd, vd = k.double().numpy(), v.double().numpy()
+            tok = 0
+            for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
+                for i in range(n):
+                    shadow[layer][(rid, c + i)] = (kd[tok], vd[tok])
+                    tok += 1
+            if check:
+                ks, vs = [], []
+                for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
+                    ks.append(np.stack([shadow[layer][(rid, p)][0] for p in range(c + n)]))
+                    vs.append(np.stack([shadow[layer][(rid, p)][1] for p in range(c + n)]))
+                ref = oa.attention_step(q.double().numpy(), q_lens, ctx_lens, ks, vs, 1 / math.sqrt(a), hq, hk)
+                assert_close(out.double().cpu().numpy(), ref, f"step {steps} layer {layer}")
+                checked += 1
+        assert lib.cb_last_error() == 0
+    assert sched.done()
+    assert checked > 20
+    if num_blocks == 16:
+        assert preempted > 0, "the tight pool is meant to exercise preemption"
