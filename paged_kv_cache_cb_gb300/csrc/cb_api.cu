@@ -56,27 +56,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Cache viewed as rows of head_dim values: [num_blocks * Hkv * block_size][A];
-// box = one (block, head) half-row group: 16 rows x 64 columns, 128-byte swizzle.
-bool encode_cache_map(CUtensorMap* m, const void* cache, int num_blocks, int n_kv_heads, int head_dim) {
+// box = `box_rows` rows x 64 columns, 128-byte swizzle: 16 rows is one (block,
+// head), 16 * Hkv rows one block of every head.
+bool encode_cache_map(CUtensorMap* m, const void* cache, int num_blocks, int n_kv_heads, int head_dim,
+                      int box_rows = kBlockSize) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * n_kv_heads * kBlockSize};
   const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// q viewed as [n_tokens][Hq][A]; box = 128/G tokens x the G heads of one group
-// x 64 columns, so one box is a 128-row query tile (row = token * G + head).
-bool encode_q_map(CUtensorMap* m, const void* q, int n_tokens, int n_q_heads, int head_dim, int group) {
+// q viewed as [n_tokens][Hq][A]; box = box_tokens tokens x box_heads heads x 64
+// columns.  Prefill: 128/G tokens x the G heads of one group, a 128-row query
+// tile (row = token * G + head); decode: 1 token x all Hq heads.
+bool encode_q_map(CUtensorMap* m, const void* q, int n_tokens, int n_q_heads, int head_dim, int box_heads,
+                  int box_tokens) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_q_heads, (cuuint64_t)n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_q_heads * head_dim * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileM / group)};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -96,7 +100,9 @@ WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int 
                                  int split_blocks) {
   WorkspaceLayout L{};
   const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
-  const long long splits = (long long)n_reqs * ((nblk + split_blocks - 1) / split_blocks);
+  // a request's blocks are cut into pieces of >= split_blocks blocks at
+  // boundaries that need not start at its first block: one piece more at most
+  const long long splits = (long long)n_reqs * ((nblk + split_blocks - 1) / split_blocks + 1);
   L.max_splits_total = (int)splits;
   size_t off = 0;
   L.counters = off;
@@ -211,19 +217,26 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
   p.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
   p.err = di.err;
 
+  const int group = n_q_heads / n_kv_heads;
+  // GQA decode with 8 KV heads: one block of all heads is one 128-row MMA tile
+  const bool block_tiles = max_q_len == 1 && head_dim == 128 && n_kv_heads == 8 && group >= 2;
+  const int box_rows = block_tiles ? n_kv_heads * kBlockSize : kBlockSize;
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_blocks, n_kv_heads, head_dim) ||
-      !encode_cache_map(&vmap, v_cache, num_blocks, n_kv_heads, head_dim))
+  if (!encode_cache_map(&kmap, k_cache, num_blocks, n_kv_heads, head_dim, box_rows) ||
+      !encode_cache_map(&vmap, v_cache, num_blocks, n_kv_heads, head_dim, box_rows))
     return CB_ECUDA;
   // split arrival counters and the work queue start at zero every call
   if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
-  const int group = n_q_heads / n_kv_heads;
   cudaError_t e;
-  if (max_q_len == 1) {
+  if (block_tiles) {
+    CUtensorMap qmap;
+    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, n_q_heads, 1)) return CB_ECUDA;
+    e = launch_decode_tcb(p, kmap, vmap, qmap, group, di.n_sms, s);
+  } else if (max_q_len == 1) {
     e = launch_decode(p, kmap, vmap, head_dim, group, di.n_sms, s);
   } else {
     CUtensorMap qmap;
-    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, group)) return CB_ECUDA;
+    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, group, kTileM / group)) return CB_ECUDA;
     e = launch_mixed(p, kmap, vmap, qmap, head_dim, group, di.n_sms, s);
   }
   if (e != cudaSuccess) return CB_ECUDA;

@@ -63,6 +63,12 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t
                              unsigned int* err, cudaStream_t stream);
 cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int head_dim,
                           int group, int n_sms, cudaStream_t stream);
+// Decode with one block of all 8 KV heads per tensor-core tile; the cache maps
+// must have 128-row boxes and the q map a box of one token's Hq heads.  It
+// cuts the work into equal pieces itself (p.split_blocks is not used); the
+// partial buffers must hold n_reqs * (ceil(max blocks / 8) + 1) splits.
+cudaError_t launch_decode_tcb(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              const CUtensorMap& qmap, int group, int n_sms, cudaStream_t stream);
 cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const CUtensorMap& qmap, int head_dim, int group, int n_sms, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);

@@ -85,6 +85,49 @@ def test_decode_only_split_k(group, head_dim):
     _parity(wl.scaled(base, ctx_lens=ctx, num_blocks=base.num_blocks + 200))
 
 
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_decode_gqa_eight_kv_heads(group):
+    """Decode-only steps with 8 KV heads, where one block of every head is one
+    128-row tensor-core tile: one key, block boundaries, one and many splits."""
+    base = wl.random_step(30 + group, n_reqs=13, max_ctx=3000, max_q=1, n_q_heads=8 * group, n_kv_heads=8,
+                          head_dim=128, p_decode=1.0)
+    ctx = list(base.ctx_lens)
+    ctx[0], ctx[1], ctx[2], ctx[3], ctx[4] = 0, 15, 16, 4095, 8190
+    _parity(wl.scaled(base, ctx_lens=ctx, num_blocks=base.num_blocks + 800))
+
+
+@pytest.mark.parametrize("group", [1, 4])
+def test_decode_running_max_rescales(group):
+    """A large softmax scale makes later blocks raise the running maximum far
+    past the lazy-rescale threshold, so the output accumulator is rescaled."""
+    base = wl.random_step(50 + group, n_reqs=6, max_ctx=2500, max_q=1, n_q_heads=8 * group, n_kv_heads=8,
+                          head_dim=128, p_decode=1.0)
+    _parity(base, scale=0.6)
+
+
+@pytest.mark.parametrize("shape", [
+    wl.random_step(61, n_reqs=9, max_ctx=900, max_q=1, n_q_heads=8, n_kv_heads=8, head_dim=128, p_decode=1.0),
+    wl.random_step(62, n_reqs=9, max_ctx=900, max_q=1, n_q_heads=32, n_kv_heads=8, head_dim=128, p_decode=1.0),
+    wl.random_step(63, n_reqs=9, max_ctx=900, max_q=1, n_q_heads=8, n_kv_heads=2, head_dim=128, p_decode=1.0),
+    wl.random_step(64, n_reqs=7, max_ctx=600, max_q=200, n_q_heads=16, n_kv_heads=8, head_dim=128, p_decode=0.5),
+    wl.random_step(65, n_reqs=7, max_ctx=600, max_q=200, n_q_heads=8, n_kv_heads=8, head_dim=64, p_decode=0.5),
+], ids=lambda s: f"{s.name}_h{s.n_q_heads}_{s.n_kv_heads}")
+def test_unwritten_cache_slots_do_not_leak(shape):
+    """Every cache slot a request does not own (past its last key in its last
+    block, and every unused block) holds NaN: outputs stay finite and equal."""
+    inp = wl.step_inputs_cpu(shape)
+    keep = torch.zeros(shape.num_blocks, shape.block_size, dtype=torch.bool)
+    for r, c in enumerate(shape.ctx_lens):
+        for p in range(c):
+            keep[int(inp["block_tables"][r, p // shape.block_size]), p % shape.block_size] = True
+    poison = ~keep[:, None, :, None]
+    for name in ("k_pool", "v_pool"):
+        inp[name] = inp[name].masked_fill(poison, float("nan"))
+    out, _, _, _ = device_step(shape, inp)
+    assert torch.isfinite(out).all()
+    assert_close(f64(out), oracle_step(shape, inp), shape.name)
+
+
 @pytest.mark.parametrize("group", [1, 4, 8])
 @pytest.mark.parametrize("head_dim", [64, 128])
 def test_chunked_prefill_tiles(group, head_dim):
@@ -143,8 +186,11 @@ def test_chunked_equals_unchunked_on_gpu():
     assert np.abs(full - chunked).max() <= 1e-2
 
 
-def test_outputs_are_deterministic():
-    shape = wl.random_step(7, n_reqs=10, max_ctx=3000, max_q=100, n_q_heads=8, n_kv_heads=2, head_dim=128)
+@pytest.mark.parametrize("shape", [
+    wl.random_step(7, n_reqs=10, max_ctx=3000, max_q=100, n_q_heads=8, n_kv_heads=2, head_dim=128),
+    wl.random_step(8, n_reqs=10, max_ctx=3000, max_q=1, n_q_heads=32, n_kv_heads=8, head_dim=128, p_decode=1.0),
+], ids=lambda s: s.name)
+def test_outputs_are_deterministic(shape):
     inp = wl.step_inputs_cpu(shape)
     o1 = device_step(shape, inp)[0]
     o2 = device_step(shape, inp)[0]
@@ -174,6 +220,22 @@ def test_block_and_tile_boundaries():
     _parity(shape)
 
 
+def test_bad_block_id_in_gqa_decode_is_reported():
+    shape = wl.random_step(71, n_reqs=5, max_ctx=600, max_q=1, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                           p_decode=1.0)
+    shape = wl.scaled(shape, ctx_lens=[300, 40, 500, 17, 250])
+    inp = wl.step_inputs_cpu(shape)
+    bad = inp["block_tables"].copy()
+    bad[1, 1] = shape.num_blocks + 5
+    bad[3, 0] = -1
+    lib = L()
+    out, _, _, status = device_step(shape, inp, check=False, attn_tables=bad)
+    assert status == lib.CB_EDEVICE
+    ref = oracle_step(shape, inp)
+    for r in (0, 2, 4):
+        assert_close(f64(out[r:r + 1]), ref[r:r + 1], f"request {r}")
+
+
 def test_bad_block_id_is_reported_not_read():
     shape = wl.tiny()
     inp = wl.step_inputs_cpu(shape)
@@ -196,13 +258,14 @@ def test_workspace_too_small_is_rejected():
         device_step(shape, inp, ws_extra=-64)
 
 
-def test_max_requests():
+@pytest.mark.parametrize("hq,hk,a", [(4, 1, 64), (64, 8, 128)])
+def test_max_requests(hq, hk, a):
     """CB_MAX_REQS decode requests with short contexts in one step."""
     lib = L()
     n = lib.CB_MAX_REQS
     rng = np.random.default_rng(3)
     ctx = tuple(int(c) for c in rng.integers(0, 40, size=n))
-    shape = wl.StepShape("max_reqs", 4, 1, 64, 16, sum(-(-(c + 1) // 16) for c in ctx) + 4,
+    shape = wl.StepShape(f"max_reqs_{hq}_{hk}", hq, hk, a, 16, sum(-(-(c + 1) // 16) for c in ctx) + 4,
                          q_lens=(1,) * n, ctx_lens=ctx, seed=9)
     _parity(shape)
 
@@ -230,6 +293,15 @@ def test_full_size_decode_llama7b_layer():
     shape = wl.decode()
     order = np.argsort(shape.ctx_lens)
     _full_size(shape, [int(order[0]), int(order[-1]), 0, 17, 40, 63])
+
+
+def test_full_size_gqa_decode_step():
+    """The 48 decodes of the mixed step alone (GQA 32/8, contexts 256..8192)."""
+    m = wl.mixed()
+    dec = [i for i, q in enumerate(m.q_lens) if q == 1]
+    shape = wl.scaled(m, name="gqa_decode48", q_lens=[1] * len(dec), ctx_lens=[m.ctx_lens[i] for i in dec])
+    order = np.argsort(shape.ctx_lens)
+    _full_size(shape, [int(order[0]), int(order[-1]), 0, 23, 47])
 
 
 def test_full_size_mixed_gqa_step():
