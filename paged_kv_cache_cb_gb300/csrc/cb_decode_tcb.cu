@@ -26,16 +26,18 @@
 //              dimension (O).  Per tile: max over the 16 tokens of a KV head by
 //              half-warp shuffles, base-2 running max with lazy rescale
 //              (> 2^8; the factors reach the O threads through shared memory),
-//              P to shared memory, per-thread partial sums.  At the end O/l, or
-//              a split partial; the split that arrives last queues the merge.
+//              P to shared memory, per-thread partial sums; at a segment's
+//              end, its row sums and maxima go to the epilogue warps.
 //   warp 4     K producer: claims chunks, publishes segments, loads the
 //              request's Hq query rows (one TMA box) and streams K tiles.
 //   warp 6     V producer: streams the published segments' V tiles, so a full
 //              V ring never holds up K loads (and the reverse).
 //   warp 5     MMA issuer (one lane), event driven: S(n) once K(n) lands,
 //              O += P(n) V(n) once P(n) and V(n) are ready.
-//   warps 7-10 merge: the split merges, queued by the softmax warps, run here
-//              while the softmax warps go on with the next segment.
+//   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
+//              last PV lands, write O/l or the split partial, and run the
+//              split merge when this split is the request's last -- all while
+//              the softmax warps go on with the next segment.
 // Every wait is bounded; the softmax warps take every stop decision at a
 // barrier that reduces it over all four warps, so none is left at a barrier.
 #include "cb_decode_item.cuh"
@@ -56,7 +58,7 @@ struct Cfg {
   static constexpr int Hq = 8 * G;
   static constexpr int KS = G == 8 ? 2 : 3;          // K ring stages
   static constexpr int VS = 2;                        // V ring stages
-  static constexpr int TM = Hq <= 32 ? 128 : 256;     // TMEM columns: S x3 and O, Hq each
+  static constexpr int TM = Hq <= 16 ? 128 : Hq <= 32 ? 256 : 512;   // TMEM columns: S x3, O x2, Hq each
 };
 
 template <int G>
@@ -79,7 +81,7 @@ struct Ctl {
   static constexpr int Hq = Cfg<G>::Hq;
   uint64_t item_full[2], item_empty[2], q_full[2], q_empty[2];
   uint64_t k_full[Cfg<G>::KS], k_empty[Cfg<G>::KS], v_full[Cfg<G>::VS], v_empty[Cfg<G>::VS];
-  uint64_t s_full[3], p_full[2], p_empty[2], o_done[2], o_free, drain;
+  uint64_t s_full[3], p_full[2], p_empty[2], o_done[2], drain;
   BItem item[2];               // the segment published in each slot (r < 0: no more work)
   int rows[2][kMaxSplitBlocks];   // its blocks' first cache rows
   struct {
@@ -87,13 +89,15 @@ struct Ctl {
     int bt[kMaxSplitBlocks];
   } raw[2];                    // an item's metadata as copied from global memory
   float alpha[2][Hq];          // per-tile rescale factors of O, per q head
-  float lsum[Hq], mmax[Hq];    // row sums / maxima at the end of an item
   float wts[Hq == 64 ? 16 : 32][Hq];   // merge: weights of a chunk of splits
   float mM[Hq], mL[Hq];        // merge: per head overall max and sum
   struct {
-    int r, t, slot0, nsplit;
-  } mq[4];                     // queued merges (r < 0: no more)
-  uint64_t mq_full[4], mq_empty[4];
+    BItem I;                   // r < 0: no more segments
+    uint32_t last_pv;
+    float lsum[Hq], mmax[Hq];  // row sums / maxima per q head
+  } ep[2];                     // finished segments handed to the epilogue warps
+  uint64_t ep_full[2], ep_empty[2], o_full[2], o_free[2];
+  int last;                    // epilogue: this split is the request's last
   int W, NC, total;             // chunk size (blocks), number of chunks, blocks in all
   int mma_nbs[4];              // MMA issuer: lengths of the segments it is between
   uint32_t tmem_base;
@@ -497,20 +501,21 @@ __device__ void b_mma(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem
     if (np < ns) {
       const int pb = np & 1, vs = np % VS;
       if (mbar_ready(&C.p_full[pb], (np >> 1) & 1) && mbar_ready(&C.v_full[vs], (np / VS) & 1) &&
-          (p_j > 0 || mbar_ready(&C.o_free, (p_it & 1) ^ 1))) {
+          (p_j > 0 || mbar_ready(&C.o_free[p_it & 1], ((p_it >> 1) & 1) ^ 1))) {
         tc_fence_after();
         const uint64_t vd = vd0 + vs * kStage, pd = pd0 + pb * kQP;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t offv = (kk * 16 * 128) >> 4;
           const uint32_t offp = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
-          tc_mma_f16(tmem + 3 * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tmem + (3 + (p_it & 1)) * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&C.o_done[np & 1]);
         tc_commit(&C.v_empty[vs]);
         tc_commit(&C.p_empty[pb]);
         ++np;
         if (++p_j == nbs[p_it & 3]) {
+          tc_commit(&C.o_full[p_it & 1]);   // the segment's O is complete once this lands
           ++p_it;
           p_j = 0;
         }
@@ -564,7 +569,7 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
   }
 }
 
-// ---------------------------------------------------------------- split merge (warps 7-10)
+// ---------------------------------------------------------------- split merge (epilogue warps)
 // Log-sum-exp merge of request r's nsplit partials (part_ml: per split and
 // head the running max m and sum l; part_acc: the unnormalised output):
 //   out[h] = sum_s 2^(m_sh - M_h) acc_sh / L_h,  M_h = max_s m_sh,
@@ -668,24 +673,7 @@ __device__ void merge_splits(const StepParams& P, Ctl<G>& C, int t, int slot0, i
   }
 }
 
-// Merge warps: run the merges the softmax warps queue, until the queue's end mark.
-template <int G>
-__device__ void b_merger(const StepParams& P, Ctl<G>& C) {
-  uint32_t nm = 0;
-  for (;;) {
-    const int q = nm & 3;
-    const bool good = wwait(P, C, &C.mq_full[q], (nm >> 2) & 1);
-    const int r = good ? C.mq[q].r : -1, t = C.mq[q].t, slot0 = C.mq[q].slot0, nsplit = C.mq[q].nsplit;
-    if (good) mbar_arrive(&C.mq_empty[q]);
-    if (named_bar_or(2, 128, !good || C.abort) || r < 0) break;
-    __threadfence();               // the other splits' partials (ordered by their counter increments)
-    merge_splits<G>(P, C, t, slot0, nsplit);
-    named_bar(2, 128);             // mM / mL / wts are rewritten by the next merge
-    ++nm;
-  }
-}
-
-// ---------------------------------------------------------------- softmax + epilogue (warps 0-3)
+// ---------------------------------------------------------------- softmax (warps 0-3)
 template <int G>
 __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
   constexpr int Hq = Cfg<G>::Hq, VS = Cfg<G>::VS;
@@ -697,7 +685,6 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
   const float sl2 = P.scale_log2;
   const int h0 = g * G;                        // this row's query heads h0 .. h0+G-1
   uint32_t it = 0, sc = 0;                     // items and tiles seen
-  uint32_t nm = 0;                             // merges queued (thread 0)
   for (;;) {
     const int slot = it & 1;
     bool good = wwait(P, C, &C.item_full[slot], (it >> 1) & 1);
@@ -776,14 +763,14 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
           if (wwait(P, C, &C.o_done[n & 1], (n >> 1) & 1)) {
             tc_fence_after();
             float o[Hq];
-            tmem_ld_n<Hq>(tmem + lane_base + 3 * Hq, o);
+            tmem_ld_n<Hq>(tmem + lane_base + (3 + (it & 1)) * Hq, o);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < Hq / 8; ++c) {
               float t8[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) t8[i] = o[c * 8 + i] * C.alpha[sb][c * 8 + i];
-              tmem_st8(tmem + lane_base + 3 * Hq + c * 8, t8);
+              tmem_st8(tmem + lane_base + (3 + (it & 1)) * Hq + c * 8, t8);
             }
             tmem_wait_st();
           }
@@ -808,63 +795,97 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
       mbar_arrive(&C.p_full[sb]);
     }
     if (stop) break;
-    // ---- epilogue: row sums per q head over the 16 rows of its KV head; O^T column per q head
+    // ---- the segment's row sums and maxima per q head (16 rows of its KV head) go to
+    // the epilogue warps, which read O when its last PV lands; this warp group
+    // goes straight on to the next segment (its PVs use the other O buffer)
+    const int e = it & 1;
+    good = wwait(P, C, &C.ep_empty[e], ((it >> 1) & 1) ^ 1);
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       float l = lp[i];
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (tok == 0) {
-        C.lsum[h0 + i] = l;
-        C.mmax[h0 + i] = m[i];
+      if (good && tok == 0) {
+        C.ep[e].lsum[h0 + i] = l;
+        C.ep[e].mmax[h0 + i] = m[i];
       }
     }
-    float o[Hq];
-    const uint32_t n = sc - 1;
-    good = wwait(P, C, &C.o_done[n & 1], (n >> 1) & 1);
-    if (good) {
-      tc_fence_after();
-      tmem_ld_n<Hq>(tmem + lane_base + 3 * Hq, o);
-      tmem_wait_ld();
+    if (good && tid == 0) {
+      C.ep[e].I = I;
+      C.ep[e].last_pv = sc - 1;
     }
-    tc_fence_before();
-    mbar_arrive(&C.o_free);
+    if (good) mbar_arrive(&C.ep_full[e]);
     if (named_bar_or(1, 128, !good || C.abort)) break;
-    const int d = tid;
+    ++it;
+  }
+  // end mark for the epilogue warps
+  if (wwait(P, C, &C.ep_empty[it & 1], ((it >> 1) & 1) ^ 1)) {
+    if (tid == 0) C.ep[it & 1].I.r = -1;
+    mbar_arrive(&C.ep_full[it & 1]);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue + merge (warps 7-10)
+// Per segment: wait until its last PV has landed in its O buffer, read O^T
+// (thread = output dimension: TMEM lane 32 * (warp % 4) + lane), free the
+// buffer, then write O/l -- or, for one split of several, the partial
+// (O, m, l); the split whose counter increment comes last merges them all.
+template <int G>
+__device__ void b_epilogue(const StepParams& P, Ctl<G>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G>::Hq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x - kMergeTid0;
+  const int d = 32 * (warp & 3) + lane;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  uint32_t k = 0;
+  for (;;) {
+    const int e = k & 1;
+    bool good = wwait(P, C, &C.ep_full[e], (k >> 1) & 1);
+    BItem I;
+    I.r = -1;
+    if (good) I = C.ep[e].I;
+    float o[Hq];
+    if (good && I.r >= 0) {
+      good = wwait(P, C, &C.o_full[e], (k >> 1) & 1);
+      if (good) {
+        tc_fence_after();
+        tmem_ld_n<Hq>(tmem + lane_base + (3 + e) * Hq, o);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(&C.o_free[e]);
+    }
+    if (named_bar_or(2, 128, !good || C.abort) || I.r < 0) break;
     if (I.nsplit == 1) {
 #pragma unroll
       for (int h = 0; h < Hq; ++h)
-        P.out[((size_t)I.t * Hq + h) * 128 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] / C.lsum[h]));
+        P.out[((size_t)I.t * Hq + h) * 128 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] / C.ep[e].lsum[h]));
     } else {
       const size_t base = (size_t)(I.slot0 + I.split) * Hq;
 #pragma unroll
       for (int h = 0; h < Hq; ++h) P.part_acc[(base + h) * 128 + d] = o[h];
       if (tid < Hq) {
-        P.part_ml[(base + tid) * 2] = C.mmax[tid];
-        P.part_ml[(base + tid) * 2 + 1] = C.lsum[tid];
-      }
-      __threadfence();
-      named_bar(1, 128);
-      if (tid == 0 && atomicAdd(P.counters + (size_t)I.r * kHkv, 1) == I.nsplit - 1) {
-        // the last split of the request: hand its merge to the merge warps
-        P.counters[(size_t)I.r * kHkv] = 0;
-        const int q = nm & 3;
-        if (lwait(P, C, &C.mq_empty[q], ((nm >> 2) & 1) ^ 1)) {
-          C.mq[q].r = I.r;
-          C.mq[q].t = I.t;
-          C.mq[q].slot0 = I.slot0;
-          C.mq[q].nsplit = I.nsplit;
-          mbar_arrive(&C.mq_full[q]);
-          ++nm;
-        }
+        P.part_ml[(base + tid) * 2] = C.ep[e].mmax[tid];
+        P.part_ml[(base + tid) * 2 + 1] = C.ep[e].lsum[tid];
       }
     }
-    named_bar(1, 128);          // lsum / mmax are rewritten by the next segment
-    ++it;
-  }
-  if (tid == 0 && lwait(P, C, &C.mq_empty[nm & 3], ((nm >> 2) & 1) ^ 1)) {   // end mark for the merge warps
-    C.mq[nm & 3].r = -1;
-    mbar_arrive(&C.mq_full[nm & 3]);
+    named_bar(2, 128);             // every thread is done with ep[e]
+    mbar_arrive(&C.ep_empty[e]);
+    if (I.nsplit > 1) {
+      __threadfence();
+      named_bar(2, 128);
+      if (tid == 0) {
+        C.last = atomicAdd(P.counters + (size_t)I.r * kHkv, 1) == I.nsplit - 1;
+        if (C.last) P.counters[(size_t)I.r * kHkv] = 0;
+      }
+      named_bar(2, 128);
+      if (C.last) {
+        __threadfence();           // the other splits' partials (ordered by their counter increments)
+        merge_splits<G>(P, C, I.t, I.slot0, I.nsplit);
+      }
+      named_bar(2, 128);           // last / mM / mL / wts are rewritten by the next segment
+    }
+    ++k;
   }
 }
 
@@ -903,11 +924,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&C.v_empty[s], 1);
     }
     for (int s = 0; s < 3; ++s) mbar_init(&C.s_full[s], 1);
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(&C.mq_full[s], 1);
-      mbar_init(&C.mq_empty[s], 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&C.ep_full[s], 128);
+      mbar_init(&C.ep_empty[s], 128);
+      mbar_init(&C.o_full[s], 1);
+      mbar_init(&C.o_free[s], 128);
     }
-    mbar_init(&C.o_free, 128);
     mbar_init(&C.drain, 1);
     C.abort = 0;
     fence_mbar_init();
@@ -929,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 6) {
     v_producer<G>(P, &vmap, T, C);
   } else if (warp >= 7) {
-    b_merger<G>(P, C);
+    b_epilogue<G>(P, C, tmem);
   } else if (warp == 5) {
     if ((threadIdx.x & 31) == 0) b_mma<G>(P, T, C, tmem);
     __syncwarp();
