@@ -218,26 +218,35 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
   p.err = di.err;
 
   const int group = n_q_heads / n_kv_heads;
-  // GQA decode with 8 KV heads: one block of all heads is one 128-row MMA tile
-  const bool block_tiles = max_q_len == 1 && head_dim == 128 && n_kv_heads == 8 && group >= 2;
-  const int box_rows = block_tiles ? n_kv_heads * kBlockSize : kBlockSize;
-  CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_blocks, n_kv_heads, head_dim, box_rows) ||
-      !encode_cache_map(&vmap, v_cache, num_blocks, n_kv_heads, head_dim, box_rows))
+  // GQA with 8 KV heads and head_dim 128: decode tokens run the block-tile
+  // pipeline (one block of all heads is one 128-row MMA tile)
+  const bool block_tiles = head_dim == 128 && n_kv_heads == 8 && group >= 2;
+  // maps: [0, 1] K, V with 16-row boxes; [2] prefill q; [3, 4] K, V with
+  // 128-row boxes; [5] decode q (one token, all heads)
+  CUtensorMap maps[6];
+  if (max_q_len > 1 || !block_tiles) {
+    if (!encode_cache_map(&maps[0], k_cache, num_blocks, n_kv_heads, head_dim, kBlockSize) ||
+        !encode_cache_map(&maps[1], v_cache, num_blocks, n_kv_heads, head_dim, kBlockSize))
+      return CB_ECUDA;
+  }
+  if (max_q_len > 1 && !encode_q_map(&maps[2], q, n_tokens, n_q_heads, head_dim, group, kTileM / group))
     return CB_ECUDA;
+  if (block_tiles) {
+    if (!encode_cache_map(&maps[3], k_cache, num_blocks, n_kv_heads, head_dim, n_kv_heads * kBlockSize) ||
+        !encode_cache_map(&maps[4], v_cache, num_blocks, n_kv_heads, head_dim, n_kv_heads * kBlockSize) ||
+        !encode_q_map(&maps[5], q, n_tokens, n_q_heads, head_dim, n_q_heads, 1))
+      return CB_ECUDA;
+  }
   // split arrival counters and the work queue start at zero every call
   if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
   cudaError_t e;
-  if (block_tiles) {
-    CUtensorMap qmap;
-    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, n_q_heads, 1)) return CB_ECUDA;
-    e = launch_decode_tcb(p, kmap, vmap, qmap, group, di.n_sms, s);
+  if (max_q_len == 1 && block_tiles) {
+    e = launch_decode_tcb(p, maps[3], maps[4], maps[5], group, di.n_sms, s);
   } else if (max_q_len == 1) {
-    e = launch_decode(p, kmap, vmap, head_dim, group, di.n_sms, s);
+    e = launch_decode(p, maps[0], maps[1], head_dim, group, di.n_sms, s);
   } else {
-    CUtensorMap qmap;
-    if (!encode_q_map(&qmap, q, n_tokens, n_q_heads, head_dim, group, kTileM / group)) return CB_ECUDA;
-    e = launch_mixed(p, kmap, vmap, qmap, head_dim, group, di.n_sms, s);
+    if (!block_tiles) maps[3] = maps[4] = maps[5] = maps[0];   // unused by the kernel
+    e = launch_mixed(p, maps, block_tiles, head_dim, group, di.n_sms, s);
   }
   if (e != cudaSuccess) return CB_ECUDA;
   g_last_launches = 1;

@@ -1,0 +1,914 @@
+// The block-tile GQA decode pipeline (8 KV heads, head_dim 128), shared by the
+// decode kernel (cb_decode_tcb.cu) and the decode phase of the mixed kernel
+// (cb_mixed.cu).
+//
+// [CB] KV cache: each request's new token attends over all its stored keys;
+// [KVN] MQA/GQA: query head h reads KV head h / G.  In the cache layout
+// [block][KV head][16 tokens][128], one block of all 8 KV heads is 128
+// contiguous rows, so a K (or V) tile is two 128-row x 64-column TMA boxes of
+// 16 KB -- an eighth of the TMA operations that per-head 16-row boxes need, and
+// exactly an M = 128 MMA operand.  Row i of a tile is (KV head i/16, token i%16).
+//     S[rows, q heads]   = K_tile . q^T                 (M=128, N=Hq, K=128 dims)
+//     O^T[dims, q heads] += V_tile^T . P^T              (M=128, N=Hq, K=128 rows)
+// P[h, row] is non-zero only where row's KV head is h/G (the GQA head mapping
+// written as a block-diagonal matrix): the off-diagonal zeros are written once
+// and the softmax threads rewrite only the diagonal entries.
+//
+// Work: the decode requests' blocks, longest request first, laid end to end
+// and cut into equal chunks of W blocks (W in [8, 32], about four chunks per
+// CTA); one CTA (11 warps) per SM, persistent, takes chunks from a global
+// counter.  A chunk is one or more segments (request r, blocks [b0, b0+nb));
+// a request cut into several segments leaves split partials that the CTA
+// finishing its last segment merges.  Equal chunks keep the CTAs' finishing
+// times together, and longest-first puts the large merges early, where they
+// overlap other CTAs' streaming, instead of at the end.  The chunk boundaries
+// depend only on the step's lengths, so results are bitwise reproducible.
+//   warps 0-3  thread = tile row (scores for its G query heads) and = output
+//              dimension (O).  Per tile: max over the 16 tokens of a KV head by
+//              half-warp shuffles, base-2 running max with lazy rescale
+//              (> 2^8; the factors reach the O threads through shared memory),
+//              P to shared memory, per-thread partial sums; at a segment's
+//              end, its row sums and maxima go to the epilogue warps.
+//   warp 4     K producer: claims chunks, publishes segments, loads the
+//              request's Hq query rows (one TMA box) and streams K tiles.
+//   warp 6     V producer: streams the published segments' V tiles, so a full
+//              V ring never holds up K loads (and the reverse).
+//   warp 5     MMA issuer (one lane), event driven: S(n) once K(n) lands,
+//              O += P(n) V(n) once P(n) and V(n) are ready.
+//   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
+//              last PV lands, write O/l or the split partial, and run the
+//              split merge when this split is the request's last -- all while
+//              the softmax warps go on with the next segment.
+// Every wait is bounded; the softmax warps take every stop decision at a
+// barrier that reduces it over all four warps, so none is left at a barrier.
+#pragma once
+#include "cb_decode_item.cuh"
+
+namespace cb {
+namespace tcb {
+
+constexpr int kThreads = 352;
+constexpr int kMergeTid0 = 224;   // merge warps 7-10
+constexpr int kHkv = 8;
+constexpr int kChunksPerCta = 4;   // work chunks per CTA (before clamping W)
+constexpr int kMinChunk = 8;       // blocks; the partial buffers are sized for it
+
+template <int G>
+struct Cfg {
+  static constexpr int Hq = 8 * G;
+  static constexpr int KS = G == 8 ? 2 : 3;          // K ring stages
+  static constexpr int VS = 2;                        // V ring stages
+  static constexpr int TM = Hq <= 16 ? 128 : Hq <= 32 ? 256 : 512;   // TMEM columns: S x3, O x2, Hq each
+};
+
+template <int G>
+struct Tiles {
+  static constexpr int Hq = Cfg<G>::Hq;
+  uint8_t k[Cfg<G>::KS][2][128][128];   // [stage][dim half][row][128 B]
+  uint8_t v[Cfg<G>::VS][2][128][128];
+  uint8_t q[2][2][Hq][128];            // [buffer][dim half][q head][128 B]
+  uint8_t p[2][2][Hq][128];            // [buffer][row half][q head][128 B]: K-major B of O^T += V^T P^T
+};
+
+// One segment: request r (query token t, kv keys), split `split` of nsplit
+// (partials at slot0 + split), blocks [b0, b0 + nb) of its table.
+struct BItem {
+  int r, split, nsplit, slot0, t, kv, b0, nb;
+};
+
+template <int G>
+struct Ctl {
+  static constexpr int Hq = Cfg<G>::Hq;
+  uint64_t item_full[2], item_empty[2], q_full[2], q_empty[2];
+  uint64_t k_full[Cfg<G>::KS], k_empty[Cfg<G>::KS], v_full[Cfg<G>::VS], v_empty[Cfg<G>::VS];
+  uint64_t s_full[3], p_full[2], p_empty[2], o_done[2], drain;
+  BItem item[2];               // the segment published in each slot (r < 0: no more work)
+  int rows[2][kMaxSplitBlocks];   // its blocks' first cache rows
+  struct {
+    int cu, ctx, pad[2];
+    int bt[kMaxSplitBlocks];
+  } raw[2];                    // an item's metadata as copied from global memory
+  float alpha[2][Hq];          // per-tile rescale factors of O, per q head
+  float wts[Hq == 64 ? 16 : 32][Hq];   // merge: weights of a chunk of splits
+  float mM[Hq], mL[Hq];        // merge: per head overall max and sum
+  struct {
+    BItem I;                   // r < 0: no more segments
+    uint32_t last_pv;
+    float lsum[Hq], mmax[Hq];  // row sums / maxima per q head
+  } ep[2];                     // finished segments handed to the epilogue warps
+  uint64_t ep_full[2], ep_empty[2], o_full[2], o_free[2];
+  int last;                    // epilogue: this split is the request's last
+  int W, NC, total;             // chunk size (blocks), number of chunks, blocks in all
+  int mma_nbs[4];              // MMA issuer: lengths of the segments it is between
+  uint32_t tmem_base;
+  volatile int abort;
+  int scratch[96];
+};
+
+// Single-thread bounded wait: on time-out records the error and raises abort.
+template <class C>
+__device__ __forceinline__ bool lwait(const StepParams& P, C& c, uint64_t* bar, uint32_t parity) {
+  if (mbar_wait(bar, parity)) return true;
+  set_error(P.err, CB_DEVERR_TIMEOUT);
+  c.abort = 1;
+  return false;
+}
+// Warp-wide bounded wait (result uniform over the warp).
+template <class C>
+__device__ __forceinline__ bool wwait(const StepParams& P, C& c, uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  if (!ok) {
+    set_error(P.err, CB_DEVERR_TIMEOUT);
+    c.abort = 1;
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------- plan (all threads)
+// Blocks of decode request r: 0 for a request with no new token and, when
+// prefill requests are allowed, for one with several; metadata that cannot be
+// right gives 0 and CB_DEVERR_BADLEN.
+__device__ __forceinline__ int decode_blocks(const StepParams& P, int r, bool allow_prefill) {
+  const int q0 = __ldg(P.cu_q_lens + r), q1 = __ldg(P.cu_q_lens + r + 1);
+  const int ctx = __ldg(P.ctx_lens + r);
+  const long long kv = (long long)ctx + 1, nblk = (kv + kBlockSize - 1) / kBlockSize;
+  if (q0 >= 0 && q1 <= P.n_tokens && (q1 - q0 == 0 || (allow_prefill && q1 - q0 > 1))) return 0;
+  if (q1 - q0 != 1 || ctx < 0 || q0 < 0 || q1 > P.n_tokens || nblk > P.max_blocks_per_seq || kv > P.max_kv_len) {
+    set_error(P.err, CB_DEVERR_BADLEN);
+    return 0;
+  }
+  return (int)nblk;
+}
+
+// Exclusive prefix sum of a[0..n) in place, a[n] = total (returned).  All
+// threads of the block call it; scratch holds >= 33 ints.
+__device__ inline int block_scan_excl(int* a, int n, int* scratch) {
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = (T + 31) >> 5;
+  const int seg = (n + T - 1) / T, lo = min(n, tid * seg), hi = min(n, lo + seg);
+  int local = 0;
+  for (int i = lo; i < hi; ++i) local += a[i];
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) scratch[wid] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int v = scratch[w];
+      scratch[w] = run;
+      run += v;
+    }
+    scratch[32] = run;
+    a[n] = run;
+  }
+  __syncthreads();
+  int run = scratch[wid] + incl - local;
+  for (int i = lo; i < hi; ++i) {
+    const int v = a[i];
+    a[i] = run;
+    run += v;
+  }
+  const int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+// Given bpre[i] = blocks of the request at position i (i < n), makes bpre the
+// exclusive prefix of blocks, picks the chunk size W (about kChunksPerCta
+// chunks per CTA, W in [kMinChunk, 32]) and makes slot the prefix of splits (a
+// request spanning chunks f..l has l - f + 1).  All threads call it; every CTA
+// computes the same plan.  Ends with __syncthreads().
+template <int G>
+__device__ void finish_plan(const StepParams& P, Ctl<G>& C, int* bpre, int* slot) {
+  const int n = P.n_reqs, tid = threadIdx.x, T = blockDim.x;
+  const int total = block_scan_excl(bpre, n, C.scratch);
+  const long long want = (total + (long long)kChunksPerCta * gridDim.x - 1) / ((long long)kChunksPerCta * gridDim.x);
+  const int W = (int)max((long long)kMinChunk, min((long long)kMaxSplitBlocks, want));
+  for (int i = tid; i < n; i += T) {
+    const int blk = bpre[i + 1] - bpre[i];
+    slot[i] = blk > 0 ? (bpre[i] + blk - 1) / W - bpre[i] / W + 1 : 0;
+  }
+  __syncthreads();
+  const int splits = block_scan_excl(slot, n, C.scratch);
+  if (tid == 0) {
+    C.W = W;
+    C.total = total;
+    C.NC = (total + W - 1) / W;
+    if (splits > P.max_splits_total) {   // cannot happen when the workspace is sized by the library
+      set_error(P.err, CB_DEVERR_BADLEN);
+      C.NC = 0;
+    }
+  }
+  __syncthreads();
+}
+
+// Barrier set-up (one thread) and P's off-diagonal zeros (all threads; the
+// caller fences and synchronises before the pipeline starts).
+template <int G>
+__device__ void init_ctl(Ctl<G>& C) {
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(&C.item_full[s], 1);
+    mbar_init(&C.item_empty[s], 1 + 128 + 1);   // MMA, softmax threads, V producer
+    mbar_init(&C.q_full[s], 1);
+    mbar_init(&C.q_empty[s], 1);
+    mbar_init(&C.p_full[s], 128);
+    mbar_init(&C.p_empty[s], 1);
+    mbar_init(&C.o_done[s], 1);
+    mbar_init(&C.ep_full[s], 128);
+    mbar_init(&C.ep_empty[s], 128);
+    mbar_init(&C.o_full[s], 1);
+    mbar_init(&C.o_free[s], 128);
+  }
+  for (int s = 0; s < Cfg<G>::KS; ++s) {
+    mbar_init(&C.k_full[s], 1);
+    mbar_init(&C.k_empty[s], 1);
+  }
+  for (int s = 0; s < Cfg<G>::VS; ++s) {
+    mbar_init(&C.v_full[s], 1);
+    mbar_init(&C.v_empty[s], 1);
+  }
+  for (int s = 0; s < 3; ++s) mbar_init(&C.s_full[s], 1);
+  mbar_init(&C.drain, 1);
+  C.abort = 0;
+}
+template <int G>
+__device__ void zero_p(Tiles<G>& T) {
+  for (int i = threadIdx.x; i < (int)sizeof(T.p) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(&T.p[0][0][0][0])[i] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------- K producer (warp 4)
+// Walks the segments of the chunks it claims.  The next segment's request
+// lengths and block-table entries are copied into shared memory (cp.async) a
+// tile or two before the current segment's last tile is issued, and the next
+// chunk is claimed (an atomic) a few tiles before that, so neither round trip
+// stalls the stream; claiming no earlier keeps the dynamic balance.
+template <int G>
+__device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* qmap, Tiles<G>& T,
+                           Ctl<G>& C, const int* order, const int* bpre, const int* slot) {
+  constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS;
+  constexpr uint32_t kTileBytes = 2 * 128 * 128;
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int n = P.n_reqs, W = C.W, NC = C.NC, total = C.total;
+  const int rows_total = P.num_blocks * kHkv * kBlockSize;
+  auto find_pos = [&](int x) {     // the position whose blocks hold linear block x
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bpre[mid] <= x)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
+  };
+  auto fetch = [&](int i, int x, int buf) {
+    const int r = order ? order[i] : i, b0 = x - bpre[i];
+    if (lane == 0) {
+      cp_async4(&C.raw[buf].cu, P.cu_q_lens + r);
+      cp_async4(&C.raw[buf].ctx, P.ctx_lens + r);
+    }
+    if (lane < W && b0 + lane < P.max_blocks_per_seq)
+      cp_async4(&C.raw[buf].bt[lane], P.block_tables + (size_t)r * P.max_blocks_per_seq + b0 + lane);
+    cp_async_commit();
+  };
+  auto claim = [&]() {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(P.queue, 1);
+    return v;                      // valid in lane 0
+  };
+  // segment cursor: chunk c (-1: none left), next linear block x, chunk end, position i
+  int c = __shfl_sync(FULL, claim(), 0), x = 0, end = 0, i = 0;
+  if (c >= NC) c = -1;
+  if (c >= 0) {
+    x = c * W;
+    end = min(x + W, total);
+    i = find_pos(x);
+    fetch(i, x, 0);
+  }
+  uint32_t it = 0, kt = 0, qt = 0;   // segments, K and q tiles issued
+  bool ok = true;
+  while (ok) {
+    const int sl = it & 1;
+    BItem I;
+    I.r = -1;
+    int y = rows_total;            // this segment's physical blocks as cache rows, one per lane
+    int seg_end = 0;
+    if (c >= 0) {
+      cp_async_wait_all();
+      __syncwarp();
+      seg_end = min(end, bpre[i + 1]);
+      I.r = order ? order[i] : i;
+      I.b0 = x - bpre[i];
+      I.nb = seg_end - x;
+      I.split = c - bpre[i] / W;
+      I.nsplit = slot[i + 1] - slot[i];
+      I.slot0 = slot[i];
+      I.t = C.raw[sl].cu;
+      I.kv = C.raw[sl].ctx + 1;
+      if (lane < I.nb) {
+        const int e = C.raw[sl].bt[lane];
+        if (e >= 0 && e < P.num_blocks)
+          y = e * kHkv * kBlockSize;
+        else
+          set_error(P.err, CB_DEVERR_BADBLOCK);   // rows past the cache read as zeros
+      }
+      __syncwarp();                // raw[sl] is refilled two segments from now
+    }
+    int good = 1;
+    if (lane == 0) {
+      good = lwait(P, C, &C.item_empty[sl], ((it >> 1) & 1) ^ 1);
+    }
+    good = __shfl_sync(FULL, good, 0);
+    if (good) C.rows[sl][lane] = y;
+    __syncwarp();
+    if (lane == 0) {
+      if (good) {
+        C.item[sl] = I;
+        mbar_arrive(&C.item_full[sl]);
+      }
+      if (good && I.r >= 0) good = lwait(P, C, &C.q_empty[sl], ((it >> 1) & 1) ^ 1);
+      if (good && I.r >= 0) {
+        mbar_arrive_expect_tx(&C.q_full[sl], 2 * Hq * 128);
+        tma_load_3d(&T.q[sl][0][0][0], qmap, 0, 0, I.t, &C.q_full[sl]);
+        tma_load_3d(&T.q[sl][1][0][0], qmap, 64, 0, I.t, &C.q_full[sl]);
+        ++qt;
+      }
+    }
+    if (!__shfl_sync(FULL, good, 0)) {
+      ok = false;
+      break;
+    }
+    if (I.r < 0) break;
+    // the next segment: the rest of this chunk, else the first of a new chunk
+    const bool chunk_done = seg_end >= end;
+    const int claim_at = chunk_done ? max(0, I.nb - 4) : -1, fetch_at = max(0, I.nb - 2);
+    // (positions with no blocks -- requests with no decode token -- are skipped)
+    int nc = c, nx = seg_end, ni = seg_end < end ? find_pos(seg_end) : i, nend = end, nraw = 0;
+    for (int j = 0; j < I.nb && ok; ++j) {
+      if (j == claim_at) nraw = claim();
+      if (j == fetch_at) {
+        if (chunk_done) {
+          nc = __shfl_sync(FULL, nraw, 0);
+          if (nc >= NC) nc = -1;
+          if (nc >= 0) {
+            nx = nc * W;
+            nend = min(nx + W, total);
+            ni = find_pos(nx);
+          }
+        }
+        if (nc >= 0) fetch(ni, nx, sl ^ 1);
+      }
+      const int yb = __shfl_sync(FULL, y, j);
+      if (lane == 0) {
+        const int ks = kt % KS;
+        good = lwait(P, C, &C.k_empty[ks], ((kt / KS) & 1) ^ 1);
+        if (good) {
+          mbar_arrive_expect_tx(&C.k_full[ks], kTileBytes);
+          tma_load_2d(&T.k[ks][0][0][0], kmap, 0, yb, &C.k_full[ks]);
+          tma_load_2d(&T.k[ks][1][0][0], kmap, 64, yb, &C.k_full[ks]);
+          ++kt;
+        }
+      }
+      ok = __shfl_sync(FULL, good, 0);
+    }
+    c = nc;
+    x = nx;
+    i = ni;
+    end = nend;
+    ++it;
+  }
+  cp_async_wait_all();             // a metadata copy still in flight lands before the CTA exits
+  if (lane == 0 && !ok) {
+    // let the tile copies already issued land before the CTA exits: at most the
+    // last KS K tiles and two q tiles can still be in flight
+    for (uint32_t k = kt > (uint32_t)KS ? kt - KS : 0; k < kt; ++k)
+      mbar_wait(&C.k_full[k % KS], (k / KS) & 1, 20000000ull);
+    for (uint32_t k = qt > 2u ? qt - 2 : 0; k < qt; ++k) mbar_wait(&C.q_full[k & 1], (k >> 1) & 1, 20000000ull);
+  }
+}
+
+// ---------------------------------------------------------------- V producer (warp 6)
+template <int G>
+__device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G>& T, Ctl<G>& C) {
+  constexpr int VS = Cfg<G>::VS;
+  constexpr uint32_t kTileBytes = 2 * 128 * 128;
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  uint32_t it = 0, vt = 0;
+  bool ok = true;
+  while (ok) {
+    const int sl = it & 1;
+    int good = 1;
+    if (lane == 0) good = lwait(P, C, &C.item_full[sl], (it >> 1) & 1);
+    if (!__shfl_sync(FULL, good, 0)) {
+      ok = false;
+      break;
+    }
+    const int r = C.item[sl].r, nb = C.item[sl].nb;
+    const int y = C.rows[sl][lane];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&C.item_empty[sl]);
+    if (r < 0) break;
+    for (int j = 0; j < nb && ok; ++j) {
+      const int yb = __shfl_sync(FULL, y, j);
+      if (lane == 0) {
+        const int vs = vt % VS;
+        good = lwait(P, C, &C.v_empty[vs], ((vt / VS) & 1) ^ 1);
+        if (good) {
+          mbar_arrive_expect_tx(&C.v_full[vs], kTileBytes);
+          tma_load_2d(&T.v[vs][0][0][0], vmap, 0, yb, &C.v_full[vs]);
+          tma_load_2d(&T.v[vs][1][0][0], vmap, 64, yb, &C.v_full[vs]);
+          ++vt;
+        }
+      }
+      ok = __shfl_sync(FULL, good, 0);
+    }
+    ++it;
+  }
+  if (lane == 0 && !ok)   // the last VS V tiles may still be in flight
+    for (uint32_t k = vt > (uint32_t)VS ? vt - VS : 0; k < vt; ++k)
+      mbar_wait(&C.v_full[k % VS], (k / VS) & 1, 20000000ull);
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 5, one lane)
+// Event driven: S(n) = K(n) q^T is issued as soon as K(n) has landed and one of
+// the three TMEM score buffers is free (S runs at most two tiles ahead of PV);
+// O += P(n) V(n) as soon as P(n) and V(n) are ready.  A late V tile then holds
+// up only its own PV, not the K stream behind it.
+template <int G>
+__device__ void b_mma(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS, VS = Cfg<G>::VS;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, Hq, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, Hq, 0, 1);   // A = V^T: MN-major
+  constexpr uint32_t kStage = (2 * 128 * 128) >> 4;              // one K/V stage, descriptor units
+  constexpr uint32_t kQP = (2 * Hq * 128) >> 4;                  // one q / P buffer
+  // K, q, P: K-major, 8-row atoms 1024 B apart.  V^T: MN-major, rows (the
+  // reduction index) 128 B apart in 1024 B atoms, the two 64-dim halves 16 KB apart.
+  const uint64_t kd0 = smem_desc_sw128(smem_u32(&T.k[0][0][0][0]), 16, 1024);
+  const uint64_t vd0 = smem_desc_sw128(smem_u32(&T.v[0][0][0][0]), 128 * 128, 1024);
+  const uint64_t qd0 = smem_desc_sw128(smem_u32(&T.q[0][0][0][0]), 16, 1024);
+  const uint64_t pd0 = smem_desc_sw128(smem_u32(&T.p[0][0][0][0]), 16, 1024);
+  uint32_t ns = 0, np = 0;         // tiles whose S / PV has been issued
+  int s_it = 0, s_j = 0, s_nb = -1;   // S cursor: segment, tile in it, its length (-1: not read yet)
+  int p_it = 0, p_j = 0;           // PV cursor
+  int* nbs = C.mma_nbs;            // lengths of the segments between the cursors (by index & 3)
+  bool s_done = false, ok = true;
+  uint64_t idle_since = 0;
+  for (;;) {
+    bool progress = false;
+    if (!s_done && s_nb < 0 && mbar_ready(&C.item_full[s_it & 1], (s_it >> 1) & 1)) {
+      const int r = C.item[s_it & 1].r, nb = C.item[s_it & 1].nb;
+      mbar_arrive(&C.item_empty[s_it & 1]);
+      if (r < 0) {
+        s_done = true;
+      } else {
+        s_nb = nb;
+        nbs[s_it & 3] = nb;
+        s_j = 0;
+      }
+      progress = true;
+    }
+    if (s_nb > 0 && ns < np + 3) {
+      const int sl = s_it & 1, ks = ns % KS;
+      if ((s_j > 0 || mbar_ready(&C.q_full[sl], (s_it >> 1) & 1)) && mbar_ready(&C.k_full[ks], (ns / KS) & 1)) {
+        tc_fence_after();
+        const uint32_t d = tmem + (ns % 3) * Hq;
+        const uint64_t kd = kd0 + ks * kStage, qd = qd0 + sl * kQP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offk = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
+          const uint32_t offq = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(d, kd + offk, qd + offq, kIdescS, kk > 0);
+        }
+        tc_commit(&C.s_full[ns % 3]);
+        tc_commit(&C.k_empty[ks]);
+        ++ns;
+        if (++s_j == s_nb) {
+          tc_commit(&C.q_empty[sl]);   // every S of this segment issued: q is free once they complete
+          ++s_it;
+          s_nb = -1;
+        }
+        progress = true;
+      }
+    }
+    if (np < ns) {
+      const int pb = np & 1, vs = np % VS;
+      if (mbar_ready(&C.p_full[pb], (np >> 1) & 1) && mbar_ready(&C.v_full[vs], (np / VS) & 1) &&
+          (p_j > 0 || mbar_ready(&C.o_free[p_it & 1], ((p_it >> 1) & 1) ^ 1))) {
+        tc_fence_after();
+        const uint64_t vd = vd0 + vs * kStage, pd = pd0 + pb * kQP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offv = (kk * 16 * 128) >> 4;
+          const uint32_t offp = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(tmem + (3 + (p_it & 1)) * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&C.o_done[np & 1]);
+        tc_commit(&C.v_empty[vs]);
+        tc_commit(&C.p_empty[pb]);
+        ++np;
+        if (++p_j == nbs[p_it & 3]) {
+          tc_commit(&C.o_full[p_it & 1]);   // the segment's O is complete once this lands
+          ++p_it;
+          p_j = 0;
+        }
+        progress = true;
+      }
+    }
+    if (s_done && np == ns) break;
+    if (progress) {
+      idle_since = 0;
+    } else {
+      const uint64_t now = globaltimer_ns();
+      if (!idle_since) {
+        idle_since = now;
+      } else if (now - idle_since > kWaitLimitNs || C.abort) {
+        set_error(P.err, CB_DEVERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok) C.abort = 1;
+  tc_commit(&C.drain);          // every MMA issued has completed before TMEM is freed
+  mbar_wait(&C.drain, 0, 20000000ull);
+}
+
+// n (8, 16, 32 or 64) consecutive TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
+  if constexpr (N == 8) {
+    float t[8];
+    tmem_ld8(taddr, t);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = t[i];
+  } else if constexpr (N == 16) {
+    float t[8], u[8];
+    tmem_ld8(taddr, t);
+    tmem_ld8(taddr + 8, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = t[i];
+      v[8 + i] = u[i];
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) {
+      float t[32];
+      tmem_ld32(taddr + c * 32, t);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[c * 32 + i] = t[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- split merge (epilogue warps)
+// Log-sum-exp merge of request r's nsplit partials (part_ml: per split and
+// head the running max m and sum l; part_acc: the unnormalised output):
+//   out[h] = sum_s 2^(m_sh - M_h) acc_sh / L_h,  M_h = max_s m_sh,
+//   L_h = sum_s 2^(m_sh - M_h) l_sh.
+// R = 128/Hq threads per head find (M, L); then per chunk of MC splits the
+// weights 2^(m - M)/L go to shared memory and each thread sums float4 partials
+// of up to 8 heads over UN splits at a time (16 float4 loads in flight).
+template <int G>
+__device__ void merge_splits(const StepParams& P, Ctl<G>& C, int t, int slot0, int nsplit) {
+  constexpr int Hq = Cfg<G>::Hq;
+  constexpr int R = 128 / Hq;        // threads per head in the (M, L) pass
+  constexpr int HT = Hq / 4;         // heads per thread in the sum
+  constexpr int HTP = HT > 8 ? 8 : HT;         // heads per thread per pass
+  constexpr int UN = 16 / HTP;                 // splits per round of loads (16 float4 in flight)
+  constexpr int MC = sizeof(C.wts) / sizeof(C.wts[0]);   // splits per weight chunk
+  const int tid = threadIdx.x - kMergeTid0, warp = tid >> 5, lane = tid & 31;
+  {
+    // a side that saw no split (M = -inf) adds nothing (and must not form -inf - -inf)
+    auto combine = [](float& M, float& L, float Mo, float Lo) {
+      const float Mn = fmaxf(M, Mo);
+      L = (M == kNegInf ? 0.f : L * ex2(M - Mn)) + (Mo == kNegInf ? 0.f : Lo * ex2(Mo - Mn));
+      M = Mn;
+    };
+    const int h = tid / R, k = tid % R;
+    const float* ml = P.part_ml + (size_t)slot0 * Hq * 2;
+    float M = kNegInf, L = 0.f;
+    for (int s0 = k; s0 < nsplit; s0 += 8 * R) {   // eight splits' loads in flight
+      float mv[8], lv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + u * R;
+        mv[u] = s < nsplit ? __ldcg(ml + ((size_t)s * Hq + h) * 2) : kNegInf;
+        lv[u] = s < nsplit ? __ldcg(ml + ((size_t)s * Hq + h) * 2 + 1) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) combine(M, L, mv[u], lv[u]);
+    }
+#pragma unroll
+    for (int off = R / 2; off > 0; off >>= 1)
+      combine(M, L, __shfl_xor_sync(0xffffffffu, M, off), __shfl_xor_sync(0xffffffffu, L, off));
+    if (k == 0) {
+      C.mM[h] = M;
+      C.mL[h] = L;
+    }
+  }
+  named_bar(2, 128);
+  // heads in passes of HTP per thread (register bound); the weights of a
+  // chunk of splits are computed once when all splits fit one chunk
+  for (int hp = 0; hp < HT; hp += HTP) {
+    float4 acc[HTP];
+#pragma unroll
+    for (int i = 0; i < HTP; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += MC) {
+      const int ns = min(MC, nsplit - s0);
+      if (hp == 0 || nsplit > MC) {
+        float mv[MC * Hq / 128];    // all of the chunk's maxima in flight at once
+#pragma unroll
+        for (int u = 0; u < MC * Hq / 128; ++u) {
+          const int e = tid + 128 * u;
+          mv[u] = e < ns * Hq ? __ldcg(P.part_ml + ((size_t)(slot0 + s0) * Hq + e) * 2) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < MC * Hq / 128; ++u) {
+          const int e = tid + 128 * u, h = e % Hq;
+          if (e < ns * Hq) C.wts[e / Hq][h] = ex2(mv[u] - C.mM[h]) / C.mL[h];
+        }
+        named_bar(2, 128);
+      }
+      for (int s = 0; s < ns; s += UN) {
+        float4 v[UN][HTP];
+#pragma unroll
+        for (int u = 0; u < UN; ++u)
+#pragma unroll
+          for (int i = 0; i < HTP; ++i)
+            if (s + u < ns)
+              v[u][i] = __ldcg(reinterpret_cast<const float4*>(
+                                   P.part_acc + ((size_t)(slot0 + s0 + s + u) * Hq + warp + 4 * (hp + i)) * 128) +
+                               lane);
+#pragma unroll
+        for (int u = 0; u < UN; ++u)
+#pragma unroll
+          for (int i = 0; i < HTP; ++i)
+            if (s + u < ns) {
+              const float w = C.wts[s + u][warp + 4 * (hp + i)];
+              acc[i].x += w * v[u][i].x;
+              acc[i].y += w * v[u][i].y;
+              acc[i].z += w * v[u][i].z;
+              acc[i].w += w * v[u][i].w;
+            }
+      }
+      if (nsplit > MC) named_bar(2, 128);   // wts is rewritten by the next chunk
+    }
+#pragma unroll
+    for (int i = 0; i < HTP; ++i) {
+      const int h = warp + 4 * (hp + i);
+      uint2 o;
+      o.x = pack_bf16(acc[i].x, acc[i].y);
+      o.y = pack_bf16(acc[i].z, acc[i].w);
+      *reinterpret_cast<uint2*>(P.out + ((size_t)t * Hq + h) * 128 + lane * 4) = o;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- softmax (warps 0-3)
+template <int G>
+__device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G>::Hq, VS = Cfg<G>::VS;
+  const int tid = threadIdx.x;                 // tile row (KV head tid/16, token tid%16); output dimension
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = tid >> 4, tok = tid & 15;
+  const bool hi = (lane >> 4) & 1;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const float sl2 = P.scale_log2;
+  const int h0 = g * G;                        // this row's query heads h0 .. h0+G-1
+  uint32_t it = 0, sc = 0;                     // items and tiles seen
+  for (;;) {
+    const int slot = it & 1;
+    bool good = wwait(P, C, &C.item_full[slot], (it >> 1) & 1);
+    BItem I;
+    I.r = -1;
+    if (good) {
+      I = C.item[slot];
+      mbar_arrive(&C.item_empty[slot]);
+    }
+    if (named_bar_or(1, 128, !good || C.abort) || I.r < 0) break;
+    float m[G], lp[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      m[i] = kNegInf;
+      lp[i] = 0.f;
+    }
+    bool stop = false;
+    for (int j = 0; j < I.nb; ++j, ++sc) {
+      const int sb = sc & 1;
+      const bool valid = (I.b0 + j) * kBlockSize + tok < I.kv;
+      bool need_any = false;
+      const int sbuf = sc % 3;    // TMEM score buffer (sb: P buffer)
+      good = wwait(P, C, &C.s_full[sbuf], (sc / 3) & 1);
+      if (good) {
+        tc_fence_after();
+        // this warp's two KV heads own columns [2*warp*G, 2*warp*G + 2G); each half-warp keeps its G
+        float sv[2 * G];
+        if constexpr (G == 2) {
+          float t8[8];
+          tmem_ld8(tmem + lane_base + sbuf * Hq + ((4 * warp) & ~7), t8);
+          tmem_wait_ld();
+          const bool upper = warp & 1;   // columns 4..7 of the 8 loaded
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sv[i] = upper ? t8[4 + i] : t8[i];
+        } else {
+          tmem_ld_n<2 * G>(tmem + lane_base + sbuf * Hq + 2 * warp * G, sv);
+          tmem_wait_ld();
+        }
+        float pv[G], alpha[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float x = valid ? (hi ? sv[G + i] : sv[i]) * sl2 : kNegInf;
+          float mx = x;
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          // every block of a split holds at least one valid token, so mx is finite
+          const bool need = mx > m[i] + 8.f;
+          alpha[i] = need ? ex2(m[i] - mx) : 1.f;
+          m[i] = need ? mx : m[i];
+          need_any |= need;
+          pv[i] = ex2(x - m[i]);
+          lp[i] = lp[i] * alpha[i] + pv[i];
+        }
+        good = wwait(P, C, &C.p_empty[sb], ((sc >> 1) & 1) ^ 1);
+        if (good) {
+          const int half = tid >> 6, c = tid & 63, chunk = c >> 3, within = (c & 7) * 2;
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            const int h = h0 + i;
+            *reinterpret_cast<__nv_bfloat16*>(&T.p[sb][half][h][((chunk ^ (h & 7)) << 4) + within]) =
+                __float2bfloat16_rn(pv[i]);
+          }
+          if (tok == 0) {
+#pragma unroll
+            for (int i = 0; i < G; ++i) C.alpha[sb][h0 + i] = alpha[i];
+          }
+        }
+      }
+      if (named_bar_or(1, 128, need_any || !good || C.abort)) {
+        if (named_bar_or(1, 128, !good || C.abort)) {
+          stop = true;
+          break;
+        }
+        if (j > 0) {   // rescale O once O += P(j-1) V(j-1) has landed
+          const uint32_t n = sc - 1;
+          if (wwait(P, C, &C.o_done[n & 1], (n >> 1) & 1)) {
+            tc_fence_after();
+            float o[Hq];
+            tmem_ld_n<Hq>(tmem + lane_base + (3 + (it & 1)) * Hq, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < Hq / 8; ++c) {
+              float t8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t8[i] = o[c * 8 + i] * C.alpha[sb][c * 8 + i];
+              tmem_st8(tmem + lane_base + (3 + (it & 1)) * Hq + c * 8, t8);
+            }
+            tmem_wait_st();
+          }
+        }
+      }
+      // value rows of tokens past the request's last key hold whatever the cache
+      // had there: each such row's thread zeroes it (0 * non-finite must not reach O)
+      if (!valid) {
+        const int vs = sc % VS;
+        if (mbar_wait(&C.v_full[vs], (sc / VS) & 1)) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(&T.v[vs][hf][tid][c << 4]) = make_uint4(0, 0, 0, 0);
+        } else {
+          set_error(P.err, CB_DEVERR_TIMEOUT);
+          C.abort = 1;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&C.p_full[sb]);
+    }
+    if (stop) break;
+    // ---- the segment's row sums and maxima per q head (16 rows of its KV head) go to
+    // the epilogue warps, which read O when its last PV lands; this warp group
+    // goes straight on to the next segment (its PVs use the other O buffer)
+    const int e = it & 1;
+    good = wwait(P, C, &C.ep_empty[e], ((it >> 1) & 1) ^ 1);
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      float l = lp[i];
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      if (good && tok == 0) {
+        C.ep[e].lsum[h0 + i] = l;
+        C.ep[e].mmax[h0 + i] = m[i];
+      }
+    }
+    if (good && tid == 0) {
+      C.ep[e].I = I;
+      C.ep[e].last_pv = sc - 1;
+    }
+    if (good) mbar_arrive(&C.ep_full[e]);
+    if (named_bar_or(1, 128, !good || C.abort)) break;
+    ++it;
+  }
+  // end mark for the epilogue warps
+  if (wwait(P, C, &C.ep_empty[it & 1], ((it >> 1) & 1) ^ 1)) {
+    if (tid == 0) C.ep[it & 1].I.r = -1;
+    mbar_arrive(&C.ep_full[it & 1]);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue + merge (warps 7-10)
+// Per segment: wait until its last PV has landed in its O buffer, read O^T
+// (thread = output dimension: TMEM lane 32 * (warp % 4) + lane), free the
+// buffer, then write O/l -- or, for one split of several, the partial
+// (O, m, l); the split whose counter increment comes last merges them all.
+template <int G>
+__device__ void b_epilogue(const StepParams& P, Ctl<G>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G>::Hq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x - kMergeTid0;
+  const int d = 32 * (warp & 3) + lane;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  uint32_t k = 0;
+  for (;;) {
+    const int e = k & 1;
+    bool good = wwait(P, C, &C.ep_full[e], (k >> 1) & 1);
+    BItem I;
+    I.r = -1;
+    if (good) I = C.ep[e].I;
+    float o[Hq];
+    if (good && I.r >= 0) {
+      good = wwait(P, C, &C.o_full[e], (k >> 1) & 1);
+      if (good) {
+        tc_fence_after();
+        tmem_ld_n<Hq>(tmem + lane_base + (3 + e) * Hq, o);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(&C.o_free[e]);
+    }
+    if (named_bar_or(2, 128, !good || C.abort) || I.r < 0) break;
+    if (I.nsplit == 1) {
+#pragma unroll
+      for (int h = 0; h < Hq; ++h)
+        P.out[((size_t)I.t * Hq + h) * 128 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] / C.ep[e].lsum[h]));
+    } else {
+      const size_t base = (size_t)(I.slot0 + I.split) * Hq;
+#pragma unroll
+      for (int h = 0; h < Hq; ++h) P.part_acc[(base + h) * 128 + d] = o[h];
+      if (tid < Hq) {
+        P.part_ml[(base + tid) * 2] = C.ep[e].mmax[tid];
+        P.part_ml[(base + tid) * 2 + 1] = C.ep[e].lsum[tid];
+      }
+    }
+    named_bar(2, 128);             // every thread is done with ep[e]
+    mbar_arrive(&C.ep_empty[e]);
+    if (I.nsplit > 1) {
+      __threadfence();
+      named_bar(2, 128);
+      if (tid == 0) {
+        C.last = atomicAdd(P.counters + (size_t)I.r * kHkv, 1) == I.nsplit - 1;
+        if (C.last) P.counters[(size_t)I.r * kHkv] = 0;
+      }
+      named_bar(2, 128);
+      if (C.last) {
+        __threadfence();           // the other splits' partials (ordered by their counter increments)
+        merge_splits<G>(P, C, I.t, I.slot0, I.nsplit);
+      }
+      named_bar(2, 128);           // last / mM / mL / wts are rewritten by the next segment
+    }
+    ++k;
+  }
+}
+
+// The decode pipeline on all kThreads threads (warp roles above) over the plan
+// (order: request at each position, nullptr for request order; bpre, slot).
+// TMEM columns [tmem, tmem + 5 Hq) must be allocated to the CTA.
+template <int G>
+__device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                             const CUtensorMap* qmap, Tiles<G>& T, Ctl<G>& C, const int* order, const int* bpre,
+                             const int* slot, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  if (warp == 4) {
+    b_producer<G>(P, kmap, qmap, T, C, order, bpre, slot);
+  } else if (warp == 6) {
+    v_producer<G>(P, vmap, T, C);
+  } else if (warp >= 7) {
+    b_epilogue<G>(P, C, tmem);
+  } else if (warp == 5) {
+    if ((threadIdx.x & 31) == 0) b_mma<G>(P, T, C, tmem);
+    __syncwarp();
+  } else {
+    b_softmax<G>(P, T, C, tmem);
+  }
+}
+
+}  // namespace tcb
+}  // namespace cb

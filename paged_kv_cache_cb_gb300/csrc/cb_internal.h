@@ -69,8 +69,11 @@ cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CU
 // partial buffers must hold n_reqs * (ceil(max blocks / 8) + 1) splits.
 cudaError_t launch_decode_tcb(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               const CUtensorMap& qmap, int group, int n_sms, cudaStream_t stream);
-cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         const CUtensorMap& qmap, int head_dim, int group, int n_sms, cudaStream_t stream);
+// Mixed prefill + decode step.  maps: K, V with 16-row boxes, the prefill q
+// map, then (block_tiles: the block-tile decode phase) K, V with 128-row boxes
+// and the decode q map.
+cudaError_t launch_mixed(const StepParams& p, const CUtensorMap* maps, bool block_tiles, int head_dim, int group,
+                         int n_sms, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
 cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream);
 

@@ -1,11 +1,13 @@
 // One launch for a mixed continuous-batching step ([CB] Continuous batching:
 // prefill chunks and decode tokens in one ragged batch).
 //
-// Persistent grid, one CTA (10 warps) per SM.  Phase 1 runs this CTA's share of
-// the prefill work (requests with more than one new token, [CB] Chunked
-// prefill) on the tensor cores; phase 2 turns eight warps into decode workers
-// that pull (request, KV head, split) items from a global counter, so CTAs that
-// finish their prefill share early absorb more decode work.
+// Persistent grid, one CTA per SM.  Phase 1 runs this CTA's share of the
+// prefill work (requests with more than one new token, [CB] Chunked prefill) on
+// the tensor cores; phase 2 serves the decode tokens from a global counter, so
+// CTAs that finish their prefill share early absorb more decode work.  Phase 2
+// is the block-tile pipeline of cb_decode_tcb.cuh (11 warps; one block of all
+// KV heads per MMA tile) when head_dim is 128, there are 8 KV heads and G >= 2,
+// else 8 warps of the CUDA-core decode workers (10 warps in all).
 //
 // Prefill item = (request r, KV head g, pair of query tiles A and B).  A query
 // tile is 128 rows = 128/G new tokens x the G query heads of group g (GQA heads
@@ -34,7 +36,7 @@
 //                         is ready, so one tile's softmax overlaps the other
 //                         tile's MMAs.
 // Every wait is bounded.
-#include "cb_decode_item.cuh"
+#include "cb_decode_tcb.cuh"
 
 namespace cb {
 
@@ -501,20 +503,43 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
   }
 }
 
-template <int A, int G>
-__global__ void __launch_bounds__(kNumThreads, 1)
+// Shared memory of the mixed kernel: the tile region (prefill tiles, or the
+// decode pipeline's rings in phase 2), the control blocks and the plan arrays.
+template <int A, int G, bool BT>
+struct MixedLayout {
+  static constexpr size_t kRegion = sizeof(PrefillTiles<A>);
+  static constexpr size_t kCtl2 = 0;
+};
+template <int G>
+struct MixedLayout<128, G, true> {
+  static constexpr size_t kRegion = sizeof(PrefillTiles<128>) > sizeof(tcb::Tiles<G>) ? sizeof(PrefillTiles<128>)
+                                                                                         : sizeof(tcb::Tiles<G>);
+  static constexpr size_t kCtl2 = sizeof(tcb::Ctl<G>);
+};
+template <int A, int G, bool BT>
+constexpr size_t mixed_smem(int n_reqs) {
+  return 1024 + MixedLayout<A, G, BT>::kRegion + sizeof(MixedCtl) + MixedLayout<A, G, BT>::kCtl2 +
+         (size_t)3 * (n_reqs + 1) * 4;
+}
+
+template <int A, int G, bool BT>
+__global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     mixed_kernel(const StepParams P, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                 const __grid_constant__ CUtensorMap qmap) {
+                 const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_b,
+                 const __grid_constant__ CUtensorMap vmap_b, const __grid_constant__ CUtensorMap qmap_d) {
   constexpr int TOK = kTileM / G;
   using WS = DecWarpSmem<A, G, kDecStages>;
+  using L = MixedLayout<A, G, BT>;
   static_assert(kDecWarps * sizeof(WS) <= sizeof(PrefillTiles<A>), "decode rings must fit in the tile region");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillTiles<A>& T = *reinterpret_cast<PrefillTiles<A>*>(base);
-  MixedCtl& C = *reinterpret_cast<MixedCtl*>(base + sizeof(PrefillTiles<A>));
-  int* dec = reinterpret_cast<int*>(base + sizeof(PrefillTiles<A>) + sizeof(MixedCtl));
-  int* spl = dec + (P.n_reqs + 1);
-  int* pre = spl + (P.n_reqs + 1);
+  MixedCtl& C = *reinterpret_cast<MixedCtl*>(base + L::kRegion);
+  // plan arrays: CUDA-core decode: dec, spl, pre; block-tile decode: pre, bpre, slot
+  int* a0 = reinterpret_cast<int*>(base + L::kRegion + sizeof(MixedCtl) + L::kCtl2);
+  int* a1 = a0 + (P.n_reqs + 1);
+  int* a2 = a1 + (P.n_reqs + 1);
+  int* pre = BT ? a0 : a2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -532,6 +557,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(&C.drain, 1);
     C.abort = 0;
+    if constexpr (BT) {
+      tcb::init_ctl<G>(*reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl)));
+      prefetch_tmap(&kmap_b);
+      prefetch_tmap(&vmap_b);
+      prefetch_tmap(&qmap_d);
+    }
     fence_mbar_init();
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
@@ -542,7 +573,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tmem_relinquish();
     tc_fence_before();
   }
-  build_plan(P, 2 * TOK, dec, spl, pre, C.scratch);     // ends with __syncthreads()
+  if constexpr (BT) {
+    // prefill items per request and decode blocks per request, both in request order
+    tcb::Ctl<G>& C2 = *reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl));
+    for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) {
+      pre[r] = request_work(P, r, 2 * TOK, true).pre_items;
+      a1[r] = tcb::decode_blocks(P, r, true);
+    }
+    __syncthreads();
+    tcb::block_scan_excl(pre, P.n_reqs, C2.scratch);
+    tcb::finish_plan<G>(P, C2, a1, a2);
+  } else {
+    build_plan(P, 2 * TOK, a0, a1, a2, C.scratch);   // ends with __syncthreads()
+  }
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
 
@@ -552,49 +595,74 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     } else if (warp == 9) {
       if (lane == 0) mma_issuer<A, G>(P, T, C, pre, tmem);
       __syncwarp();
-    } else {
+    } else if (warp < 8) {
       softmax_side<A, G>(P, T, C, pre, tmem, warp >> 2);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if constexpr (BT) {
+    // phase 2: the tile region becomes the decode pipeline's rings
+    tcb::Tiles<G>& T2 = *reinterpret_cast<tcb::Tiles<G>*>(base);
+    tcb::Ctl<G>& C2 = *reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl));
+    tcb::zero_p<G>(T2);
+    fence_proxy_async_smem();
+    __syncthreads();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if (!C.abort) tcb::run_pipeline<G>(P, &kmap_b, &vmap_b, &qmap_d, T2, C2, nullptr, a1, a2, tmem);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+  } else {
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    if (C.abort || warp >= kDecWarps) return;
+    decode_worker<A, G, kDecStages, 2>(P, &kmap, &vmap, reinterpret_cast<WS*>(base)[warp], a0, a1);
   }
-  if (C.abort || warp >= kDecWarps) return;
-  decode_worker<A, G, kDecStages, 2>(P, &kmap, &vmap, reinterpret_cast<WS*>(base)[warp], dec, spl);
 }
+static_assert(mixed_smem<128, 2, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 4, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 8, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 
-template <int A, int G>
-cudaError_t launch_mixed_t(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& qmap, int n_sms, cudaStream_t stream) {
-  const size_t smem = 1024 + sizeof(PrefillTiles<A>) + sizeof(MixedCtl) + (size_t)3 * (p.n_reqs + 1) * 4;
+template <int A, int G, bool BT>
+cudaError_t launch_mixed_t(const StepParams& p, const CUtensorMap* maps, int n_sms, cudaStream_t stream) {
+  const size_t smem = mixed_smem<A, G, BT>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mixed_kernel<A, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e =
+        cudaFuncSetAttribute(mixed_kernel<A, G, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  mixed_kernel<A, G><<<n_sms, kNumThreads, smem, stream>>>(p, kmap, vmap, qmap);
+  mixed_kernel<A, G, BT><<<n_sms, BT ? tcb::kThreads : kNumThreads, smem, stream>>>(p, maps[0], maps[1], maps[2],
+                                                                                     maps[3], maps[4], maps[5]);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         const CUtensorMap& qmap, int head_dim, int group, int n_sms, cudaStream_t stream) {
-#define CB_MIX_CASE(A_, G_) \
-  if (head_dim == A_ && group == G_) return launch_mixed_t<A_, G_>(p, kmap, vmap, qmap, n_sms, stream);
-  CB_MIX_CASE(128, 1)
-  CB_MIX_CASE(128, 2)
-  CB_MIX_CASE(128, 4)
-  CB_MIX_CASE(128, 8)
-  CB_MIX_CASE(64, 1)
-  CB_MIX_CASE(64, 2)
-  CB_MIX_CASE(64, 4)
-  CB_MIX_CASE(64, 8)
+cudaError_t launch_mixed(const StepParams& p, const CUtensorMap* maps, bool block_tiles, int head_dim, int group,
+                         int n_sms, cudaStream_t stream) {
+#define CB_MIX_CASE(A_, G_, BT_)                  \
+  if (head_dim == A_ && group == G_ && block_tiles == BT_) \
+    return launch_mixed_t<A_, G_, BT_>(p, maps, n_sms, stream);
+  CB_MIX_CASE(128, 2, true)
+  CB_MIX_CASE(128, 4, true)
+  CB_MIX_CASE(128, 8, true)
+  CB_MIX_CASE(128, 1, false)
+  CB_MIX_CASE(128, 2, false)
+  CB_MIX_CASE(128, 4, false)
+  CB_MIX_CASE(128, 8, false)
+  CB_MIX_CASE(64, 1, false)
+  CB_MIX_CASE(64, 2, false)
+  CB_MIX_CASE(64, 4, false)
+  CB_MIX_CASE(64, 8, false)
 #undef CB_MIX_CASE
   return cudaErrorInvalidValue;
 }

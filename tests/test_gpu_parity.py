@@ -148,6 +148,19 @@ def test_random_mixed_steps(seed):
     _parity(shape)
 
 
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_mixed_steps_eight_kv_heads(group):
+    """Mixed prefill + decode steps with 8 KV heads and head_dim 128: the decode
+    tokens run the block-tile phase of the mixed kernel."""
+    shape = wl.random_step(200 + group, n_reqs=14, max_ctx=2500, max_q=300, n_q_heads=8 * group, n_kv_heads=8,
+                           head_dim=128, p_decode=0.7)
+    q, c = list(shape.q_lens), list(shape.ctx_lens)
+    q[0], c[0] = 1, 0              # a decode with a single key
+    q[1], c[1] = 1, 4100           # a decode cut into several splits
+    q[2], c[2] = 77, 15            # a prefill chunk after a partial block
+    _parity(wl.scaled(shape, q_lens=q, ctx_lens=c, num_blocks=shape.num_blocks + 400))
+
+
 def test_scale_argument_is_honoured():
     _parity(wl.tiny(), scale=0.05)
 

@@ -21,13 +21,13 @@ def _bf16(rng, shape):
     return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("seed,num_blocks,head_dim", [(1, 16, 64), (2, 20, 128)])
-def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim):
+@pytest.mark.parametrize("seed,num_blocks,head_dim,hq,hk", [(1, 16, 64, 8, 2), (2, 20, 128, 8, 2), (3, 18, 128, 32, 8)])
+def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = L()
     tr = wl.small_trace(seed, num_blocks=num_blocks)
-    hq, hk, a, bs, nl = 8, 2, head_dim, tr.block_size, 2
+    a, bs, nl = head_dim, tr.block_size, 2
     maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
     max_seq = max(p + o - 1 for _, p, o in tr.requests)
     sched = lib.Scheduler(tr.num_blocks, bs, tr.token_budget, tr.token_budget, wl.free_order(tr.num_blocks, tr.seed),
