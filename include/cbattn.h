@@ -87,9 +87,13 @@ int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mappi
  *     out[t][h] = softmax_j(scale * q[t][h] . K[j]) . V[j],   j <= ctx + i.
  * The new tokens' keys must already be in the cache (cb_kv_append).  Requests
  * never see each other's keys (the block-diagonal ragged mask).
- * Decode requests (q_len == 1) run on CUDA cores, split over KV blocks, with the
- * splits merged by log-sum-exp; requests with q_len > 1 run as 128-row tiles on
- * the tensor cores.  Everything is one kernel launch (plus a memset of the
+ * Requests with q_len > 1 run as 128-row tiles on the tensor cores.  Decode
+ * requests (q_len == 1) are split over their KV blocks and the splits merged by
+ * log-sum-exp: with 8 KV heads and head_dim 128 on the tensor cores (one
+ * physical block of all heads per MMA tile; the merge runs on the whole grid
+ * after a grid-wide barrier, so that launch is cooperative and fails with
+ * CB_ECUDA if the device cannot hold one CTA on every SM at once), otherwise on
+ * CUDA cores.  Everything is one kernel launch (plus a memset of the
  * workspace's counters).
  *
  *  q              device, bf16 [n_tokens][n_q_heads][head_dim]

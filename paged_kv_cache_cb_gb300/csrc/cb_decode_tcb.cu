@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg<G>::TM);
   }
+  merge_phase<G>(P, C, order, slot);
 }
 
 template <int G>
@@ -121,8 +122,12 @@ cudaError_t launch_t(const StepParams& p, const CUtensorMap& kmap, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_tcb_kernel<G><<<n_sms, kThreads, smem, stream>>>(p, kmap, vmap, qmap);
-  return cudaGetLastError();
+  // cooperative: the merge phase waits for every CTA
+  StepParams pc = p;
+  void* args[] = {&pc, const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap),
+                  const_cast<CUtensorMap*>(&qmap)};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(decode_tcb_kernel<G>), dim3(n_sms), dim3(kThreads),
+                                     args, smem, stream);
 }
 
 }  // namespace

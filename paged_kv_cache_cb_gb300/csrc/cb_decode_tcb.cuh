@@ -18,11 +18,10 @@
 // and cut into equal chunks of W blocks (W in [8, 32], about four chunks per
 // CTA); one CTA (11 warps) per SM, persistent, takes chunks from a global
 // counter.  A chunk is one or more segments (request r, blocks [b0, b0+nb));
-// a request cut into several segments leaves split partials that the CTA
-// finishing its last segment merges.  Equal chunks keep the CTAs' finishing
-// times together, and longest-first puts the large merges early, where they
-// overlap other CTAs' streaming, instead of at the end.  The chunk boundaries
-// depend only on the step's lengths, so results are bitwise reproducible.
+// a request cut into several segments leaves split partials, merged by the
+// whole grid once every chunk is done.  Equal chunks keep the CTAs' finishing
+// times together.  The chunk boundaries depend only on the step's lengths, so
+// results are bitwise reproducible.
 //   warps 0-3  thread = tile row (scores for its G query heads) and = output
 //              dimension (O).  Per tile: max over the 16 tokens of a KV head by
 //              half-warp shuffles, base-2 running max with lazy rescale
@@ -36,9 +35,10 @@
 //   warp 5     MMA issuer (one lane), event driven: S(n) once K(n) lands,
 //              O += P(n) V(n) once P(n) and V(n) are ready.
 //   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
-//              last PV lands, write O/l or the split partial, and run the
-//              split merge when this split is the request's last -- all while
-//              the softmax warps go on with the next segment.
+//              last PV lands and write O/l or the split partial, while the
+//              softmax warps go on with the next segment.
+// After the pipeline, a grid-wide barrier and a merge phase in which every warp
+// of the grid merges (request, head) pairs of the requests cut into splits.
 // Every wait is bounded; the softmax warps take every stop decision at a
 // barrier that reduces it over all four warps, so none is left at a barrier.
 #pragma once
@@ -48,7 +48,7 @@ namespace cb {
 namespace tcb {
 
 constexpr int kThreads = 352;
-constexpr int kMergeTid0 = 224;   // merge warps 7-10
+constexpr int kMergeTid0 = 224;   // epilogue warps 7-10
 constexpr int kHkv = 8;
 constexpr int kChunksPerCta = 4;   // work chunks per CTA (before clamping W)
 constexpr int kMinChunk = 8;       // blocks; the partial buffers are sized for it
@@ -89,15 +89,13 @@ struct Ctl {
     int bt[kMaxSplitBlocks];
   } raw[2];                    // an item's metadata as copied from global memory
   float alpha[2][Hq];          // per-tile rescale factors of O, per q head
-  float wts[Hq == 64 ? 16 : 32][Hq];   // merge: weights of a chunk of splits
-  float mM[Hq], mL[Hq];        // merge: per head overall max and sum
   struct {
     BItem I;                   // r < 0: no more segments
     uint32_t last_pv;
     float lsum[Hq], mmax[Hq];  // row sums / maxima per q head
   } ep[2];                     // finished segments handed to the epilogue warps
   uint64_t ep_full[2], ep_empty[2], o_full[2], o_free[2];
-  int last;                    // epilogue: this split is the request's last
+  int merge_ok;                // every CTA reached the merge barrier in time
   int W, NC, total;             // chunk size (blocks), number of chunks, blocks in all
   int mma_nbs[4];              // MMA issuer: lengths of the segments it is between
   uint32_t tmem_base;
@@ -568,110 +566,6 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
   }
 }
 
-// ---------------------------------------------------------------- split merge (epilogue warps)
-// Log-sum-exp merge of request r's nsplit partials (part_ml: per split and
-// head the running max m and sum l; part_acc: the unnormalised output):
-//   out[h] = sum_s 2^(m_sh - M_h) acc_sh / L_h,  M_h = max_s m_sh,
-//   L_h = sum_s 2^(m_sh - M_h) l_sh.
-// R = 128/Hq threads per head find (M, L); then per chunk of MC splits the
-// weights 2^(m - M)/L go to shared memory and each thread sums float4 partials
-// of up to 8 heads over UN splits at a time (16 float4 loads in flight).
-template <int G>
-__device__ void merge_splits(const StepParams& P, Ctl<G>& C, int t, int slot0, int nsplit) {
-  constexpr int Hq = Cfg<G>::Hq;
-  constexpr int R = 128 / Hq;        // threads per head in the (M, L) pass
-  constexpr int HT = Hq / 4;         // heads per thread in the sum
-  constexpr int HTP = HT > 8 ? 8 : HT;         // heads per thread per pass
-  constexpr int UN = 16 / HTP;                 // splits per round of loads (16 float4 in flight)
-  constexpr int MC = sizeof(C.wts) / sizeof(C.wts[0]);   // splits per weight chunk
-  const int tid = threadIdx.x - kMergeTid0, warp = tid >> 5, lane = tid & 31;
-  {
-    // a side that saw no split (M = -inf) adds nothing (and must not form -inf - -inf)
-    auto combine = [](float& M, float& L, float Mo, float Lo) {
-      const float Mn = fmaxf(M, Mo);
-      L = (M == kNegInf ? 0.f : L * ex2(M - Mn)) + (Mo == kNegInf ? 0.f : Lo * ex2(Mo - Mn));
-      M = Mn;
-    };
-    const int h = tid / R, k = tid % R;
-    const float* ml = P.part_ml + (size_t)slot0 * Hq * 2;
-    float M = kNegInf, L = 0.f;
-    for (int s0 = k; s0 < nsplit; s0 += 8 * R) {   // eight splits' loads in flight
-      float mv[8], lv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int s = s0 + u * R;
-        mv[u] = s < nsplit ? __ldcg(ml + ((size_t)s * Hq + h) * 2) : kNegInf;
-        lv[u] = s < nsplit ? __ldcg(ml + ((size_t)s * Hq + h) * 2 + 1) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) combine(M, L, mv[u], lv[u]);
-    }
-#pragma unroll
-    for (int off = R / 2; off > 0; off >>= 1)
-      combine(M, L, __shfl_xor_sync(0xffffffffu, M, off), __shfl_xor_sync(0xffffffffu, L, off));
-    if (k == 0) {
-      C.mM[h] = M;
-      C.mL[h] = L;
-    }
-  }
-  named_bar(2, 128);
-  // heads in passes of HTP per thread (register bound); the weights of a
-  // chunk of splits are computed once when all splits fit one chunk
-  for (int hp = 0; hp < HT; hp += HTP) {
-    float4 acc[HTP];
-#pragma unroll
-    for (int i = 0; i < HTP; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nsplit; s0 += MC) {
-      const int ns = min(MC, nsplit - s0);
-      if (hp == 0 || nsplit > MC) {
-        float mv[MC * Hq / 128];    // all of the chunk's maxima in flight at once
-#pragma unroll
-        for (int u = 0; u < MC * Hq / 128; ++u) {
-          const int e = tid + 128 * u;
-          mv[u] = e < ns * Hq ? __ldcg(P.part_ml + ((size_t)(slot0 + s0) * Hq + e) * 2) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < MC * Hq / 128; ++u) {
-          const int e = tid + 128 * u, h = e % Hq;
-          if (e < ns * Hq) C.wts[e / Hq][h] = ex2(mv[u] - C.mM[h]) / C.mL[h];
-        }
-        named_bar(2, 128);
-      }
-      for (int s = 0; s < ns; s += UN) {
-        float4 v[UN][HTP];
-#pragma unroll
-        for (int u = 0; u < UN; ++u)
-#pragma unroll
-          for (int i = 0; i < HTP; ++i)
-            if (s + u < ns)
-              v[u][i] = __ldcg(reinterpret_cast<const float4*>(
-                                   P.part_acc + ((size_t)(slot0 + s0 + s + u) * Hq + warp + 4 * (hp + i)) * 128) +
-                               lane);
-#pragma unroll
-        for (int u = 0; u < UN; ++u)
-#pragma unroll
-          for (int i = 0; i < HTP; ++i)
-            if (s + u < ns) {
-              const float w = C.wts[s + u][warp + 4 * (hp + i)];
-              acc[i].x += w * v[u][i].x;
-              acc[i].y += w * v[u][i].y;
-              acc[i].z += w * v[u][i].z;
-              acc[i].w += w * v[u][i].w;
-            }
-      }
-      if (nsplit > MC) named_bar(2, 128);   // wts is rewritten by the next chunk
-    }
-#pragma unroll
-    for (int i = 0; i < HTP; ++i) {
-      const int h = warp + 4 * (hp + i);
-      uint2 o;
-      o.x = pack_bf16(acc[i].x, acc[i].y);
-      o.y = pack_bf16(acc[i].z, acc[i].w);
-      *reinterpret_cast<uint2*>(P.out + ((size_t)t * Hq + h) * 128 + lane * 4) = o;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- softmax (warps 0-3)
 template <int G>
 __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
@@ -824,11 +718,11 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
   }
 }
 
-// ---------------------------------------------------------------- epilogue + merge (warps 7-10)
+// ---------------------------------------------------------------- epilogue (warps 7-10)
 // Per segment: wait until its last PV has landed in its O buffer, read O^T
 // (thread = output dimension: TMEM lane 32 * (warp % 4) + lane), free the
 // buffer, then write O/l -- or, for one split of several, the partial
-// (O, m, l); the split whose counter increment comes last merges them all.
+// (O, m, l) for the merge phase.
 template <int G>
 __device__ void b_epilogue(const StepParams& P, Ctl<G>& C, uint32_t tmem) {
   constexpr int Hq = Cfg<G>::Hq;
@@ -870,21 +764,87 @@ __device__ void b_epilogue(const StepParams& P, Ctl<G>& C, uint32_t tmem) {
     }
     named_bar(2, 128);             // every thread is done with ep[e]
     mbar_arrive(&C.ep_empty[e]);
-    if (I.nsplit > 1) {
-      __threadfence();
-      named_bar(2, 128);
-      if (tid == 0) {
-        C.last = atomicAdd(P.counters + (size_t)I.r * kHkv, 1) == I.nsplit - 1;
-        if (C.last) P.counters[(size_t)I.r * kHkv] = 0;
-      }
-      named_bar(2, 128);
-      if (C.last) {
-        __threadfence();           // the other splits' partials (ordered by their counter increments)
-        merge_splits<G>(P, C, I.t, I.slot0, I.nsplit);
-      }
-      named_bar(2, 128);           // last / mM / mL / wts are rewritten by the next segment
-    }
     ++k;
+  }
+}
+
+// ---------------------------------------------------------------- split merge (all warps of the grid)
+__device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// After the pipeline: a grid-wide barrier (the launch is cooperative, so every
+// CTA is resident; the wait is bounded), then every warp of the grid merges one
+// (request, q head) of the requests cut into several splits at a time, by
+// log-sum-exp over the splits' partials (m: running max, l: sum, acc: O):
+//   out = sum_s 2^(m_s - M) acc_s / L,  M = max_s m_s,  L = sum_s 2^(m_s - M) l_s.
+// Lane = 4 output dimensions; eight splits' loads in flight.  All threads of
+// the CTA call it.
+template <int G>
+__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* order, const int* slot) {
+  constexpr int Hq = Cfg<G>::Hq;
+  const unsigned FULL = 0xffffffffu;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    C.merge_ok = 1;
+    __threadfence();               // this CTA's partials before its arrival
+    atomicAdd(P.queue + 1, 1);
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(P.queue + 1) < gridDim.x) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(P.err, CB_DEVERR_TIMEOUT);
+        C.merge_ok = 0;
+        break;
+      }
+      __nanosleep(200);
+    }
+  }
+  __syncthreads();
+  if (!C.merge_ok) return;
+  const int nw = blockDim.x >> 5;
+  const int n_task = P.n_reqs * Hq;
+  for (int task = blockIdx.x * nw + warp; task < n_task; task += gridDim.x * nw) {
+    const int i = task / Hq, h = task - i * Hq;
+    const int slot0 = slot[i], ns = slot[i + 1] - slot0;
+    if (ns <= 1) continue;
+    const float* ml = P.part_ml + ((size_t)slot0 * Hq + h) * 2;
+    float M = kNegInf;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(ml + (size_t)s * Hq * 2));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+    float L = 0.f;
+    for (int s = lane; s < ns; s += 32) L += ex2(__ldcg(ml + (size_t)s * Hq * 2) - M) * __ldcg(ml + (size_t)s * Hq * 2 + 1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
+    const float inv = 1.f / L;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(P.part_acc + ((size_t)slot0 * Hq + h) * 128) + lane;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const int cnt = min(32, ns - s0);
+      const float w_lane = lane < cnt ? ex2(__ldcg(ml + (size_t)(s0 + lane) * Hq * 2) - M) * inv : 0.f;
+      for (int u = 0; u < cnt; u += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = u + k < cnt ? __ldcg(src + (size_t)(s0 + u + k) * Hq * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float w = __shfl_sync(FULL, w_lane, (u + k) & 31);
+          acc.x += w * v[k].x;
+          acc.y += w * v[k].y;
+          acc.z += w * v[k].z;
+          acc.w += w * v[k].w;
+        }
+      }
+    }
+    const int t = __ldg(P.cu_q_lens + (order ? order[i] : i));
+    uint2 o;
+    o.x = pack_bf16(acc.x, acc.y);
+    o.y = pack_bf16(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(P.out + ((size_t)t * Hq + h) * 128 + lane * 4) = o;
   }
 }
 

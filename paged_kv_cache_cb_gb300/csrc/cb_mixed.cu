@@ -616,6 +616,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
+    tcb::merge_phase<G>(P, C2, nullptr, a2);
   } else {
     if (warp == 9) {
       tc_fence_after();
@@ -640,9 +641,18 @@ cudaError_t launch_mixed_t(const StepParams& p, const CUtensorMap* maps, int n_s
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  mixed_kernel<A, G, BT><<<n_sms, BT ? tcb::kThreads : kNumThreads, smem, stream>>>(p, maps[0], maps[1], maps[2],
-                                                                                     maps[3], maps[4], maps[5]);
-  return cudaGetLastError();
+  if constexpr (BT) {   // cooperative: the decode merge phase waits for every CTA
+    StepParams pc = p;
+    void* args[] = {&pc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
+                    const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
+                    const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5])};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), dim3(n_sms),
+                                       dim3(tcb::kThreads), args, smem, stream);
+  } else {
+    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                                   maps[5]);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
