@@ -14,8 +14,8 @@
 // written as a block-diagonal matrix): the off-diagonal zeros are written once
 // and the softmax threads rewrite only the diagonal entries.
 //
-// Work: the decode requests' blocks, longest request first, laid end to end
-// and cut into equal chunks of W blocks (W in [8, 32], about four chunks per
+// Work: the decode requests' blocks, laid end to end in request order and cut
+// into equal chunks of W blocks (W in [8, 32], about four chunks per
 // CTA); one CTA (11 warps) per SM, persistent, takes chunks from a global
 // counter.  A chunk is one or more segments (request r, blocks [b0, b0+nb));
 // a request cut into several segments leaves split partials, merged by the
@@ -175,8 +175,8 @@ __device__ inline int block_scan_excl(int* a, int n, int* scratch) {
   return total;
 }
 
-// Given bpre[i] = blocks of the request at position i (i < n), makes bpre the
-// exclusive prefix of blocks, picks the chunk size W (about kChunksPerCta
+// Given bpre[r] = decode blocks of request r (r < n), makes bpre the exclusive
+// prefix of blocks, picks the chunk size W (about kChunksPerCta
 // chunks per CTA, W in [kMinChunk, 32]) and makes slot the prefix of splits (a
 // request spanning chunks f..l has l - f + 1).  All threads call it; every CTA
 // computes the same plan.  Ends with __syncthreads().
@@ -247,14 +247,14 @@ __device__ void zero_p(Tiles<G>& T) {
 // stalls the stream; claiming no earlier keeps the dynamic balance.
 template <int G>
 __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* qmap, Tiles<G>& T,
-                           Ctl<G>& C, const int* order, const int* bpre, const int* slot) {
+                           Ctl<G>& C, const int* bpre, const int* slot) {
   constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS;
   constexpr uint32_t kTileBytes = 2 * 128 * 128;
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int n = P.n_reqs, W = C.W, NC = C.NC, total = C.total;
   const int rows_total = P.num_blocks * kHkv * kBlockSize;
-  auto find_pos = [&](int x) {     // the position whose blocks hold linear block x
+  auto find_pos = [&](int x) {     // the request whose blocks hold linear block x
     int lo = 0, hi = n - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -266,7 +266,7 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     return lo;
   };
   auto fetch = [&](int i, int x, int buf) {
-    const int r = order ? order[i] : i, b0 = x - bpre[i];
+    const int r = i, b0 = x - bpre[i];
     if (lane == 0) {
       cp_async4(&C.raw[buf].cu, P.cu_q_lens + r);
       cp_async4(&C.raw[buf].ctx, P.ctx_lens + r);
@@ -280,7 +280,7 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     if (lane == 0) v = atomicAdd(P.queue, 1);
     return v;                      // valid in lane 0
   };
-  // segment cursor: chunk c (-1: none left), next linear block x, chunk end, position i
+  // segment cursor: chunk c (-1: none left), next linear block x, chunk end, request i
   int c = __shfl_sync(FULL, claim(), 0), x = 0, end = 0, i = 0;
   if (c >= NC) c = -1;
   if (c >= 0) {
@@ -301,7 +301,7 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
       cp_async_wait_all();
       __syncwarp();
       seg_end = min(end, bpre[i + 1]);
-      I.r = order ? order[i] : i;
+      I.r = i;
       I.b0 = x - bpre[i];
       I.nb = seg_end - x;
       I.split = c - bpre[i] / W;
@@ -346,7 +346,7 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     // the next segment: the rest of this chunk, else the first of a new chunk
     const bool chunk_done = seg_end >= end;
     const int claim_at = chunk_done ? max(0, I.nb - 4) : -1, fetch_at = max(0, I.nb - 2);
-    // (positions with no blocks -- requests with no decode token -- are skipped)
+    // (requests with no decode token have no blocks and are skipped)
     int nc = c, nx = seg_end, ni = seg_end < end ? find_pos(seg_end) : i, nend = end, nraw = 0;
     for (int j = 0; j < I.nb && ok; ++j) {
       if (j == claim_at) nraw = claim();
@@ -783,7 +783,7 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
 // Lane = 4 output dimensions; eight splits' loads in flight.  All threads of
 // the CTA call it.
 template <int G>
-__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* order, const int* slot) {
+__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* slot) {
   constexpr int Hq = Cfg<G>::Hq;
   const unsigned FULL = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -840,7 +840,7 @@ __device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* order, co
         }
       }
     }
-    const int t = __ldg(P.cu_q_lens + (order ? order[i] : i));
+    const int t = __ldg(P.cu_q_lens + i);
     uint2 o;
     o.x = pack_bf16(acc.x, acc.y);
     o.y = pack_bf16(acc.z, acc.w);
@@ -849,15 +849,15 @@ __device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* order, co
 }
 
 // The decode pipeline on all kThreads threads (warp roles above) over the plan
-// (order: request at each position, nullptr for request order; bpre, slot).
+// (bpre, slot of finish_plan).
 // TMEM columns [tmem, tmem + 5 Hq) must be allocated to the CTA.
 template <int G>
 __device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                             const CUtensorMap* qmap, Tiles<G>& T, Ctl<G>& C, const int* order, const int* bpre,
-                             const int* slot, uint32_t tmem) {
+                             const CUtensorMap* qmap, Tiles<G>& T, Ctl<G>& C, const int* bpre, const int* slot,
+                             uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
   if (warp == 4) {
-    b_producer<G>(P, kmap, qmap, T, C, order, bpre, slot);
+    b_producer<G>(P, kmap, qmap, T, C, bpre, slot);
   } else if (warp == 6) {
     v_producer<G>(P, vmap, T, C);
   } else if (warp >= 7) {
