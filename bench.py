@@ -43,11 +43,14 @@ WORKLOADS = {
               "mixed: 48 decodes ctx U[256,8192] + 2x512-token chunks after 1024/3072, GQA 32/8 x128, bf16"),
     "mixed_budget": (lambda seed, pool=20: wl.mixed(seed=seed, budget_variant=True, pool_bytes=pool * wl.GB),
                      "mixed, 560-token budget: 48 decodes + one 512-token chunk after 1024, GQA 32/8 x128"),
+    "gqa_decode": (lambda seed, pool=20: wl.gqa_decode(seed=seed, pool_bytes=pool * wl.GB),
+                   "gqa_decode: the mixed step's 48 decodes alone, ctx U[256,8192], GQA 32/8 x128, bf16"),
     "long": (lambda seed, pool=20: wl.long(15, seed=seed, pool_bytes=pool * wl.GB),
              "long: 2048-token chunk after 30720 stored (step 15 of a 32768 prompt) + 16 decodes at 8207, GQA 32/8"),
     "tiny": (lambda seed, pool=20: wl.tiny(seed=seed), "tiny: 4 requests (37,1),(100,1),(4,3),(0,20), MHA 4x64"),
 }
-KERNEL_SOURCES = ["cb_common.cuh", "cb_decode_item.cuh", "cb_decode.cu", "cb_mixed.cu", "cb_api.cu"]
+KERNEL_SOURCES = ["cb_common.cuh", "cb_decode_item.cuh", "cb_decode.cu", "cb_decode_tcb.cuh", "cb_decode_tcb.cu",
+                  "cb_mixed.cu", "cb_api.cu"]
 
 
 # ---------------------------------------------------------------- work accounting

@@ -87,6 +87,15 @@ def mixed(seed=0, budget_variant=False, pool_bytes=20 * GB):
                      pool_blocks(pool_bytes, 8, 128), q_lens=tuple(q), ctx_lens=tuple(ctx), seed=seed)
 
 
+def gqa_decode(seed=0, pool_bytes=20 * GB):
+    """The decode requests of ``mixed`` alone: a decode-only step of 48 requests,
+    GQA 32/8 x 128, ctx U[256, 8192] (same seed, same lengths)."""
+    m = mixed(seed=seed, pool_bytes=pool_bytes)
+    ctx = [c for c, q in zip(m.ctx_lens, m.q_lens) if q == 1]
+    return StepShape("gqa_decode", m.n_q_heads, m.n_kv_heads, m.head_dim, m.block_size, m.num_blocks,
+                     (1,) * len(ctx), tuple(ctx), m.seed)
+
+
 def long(k=15, seed=0, pool_bytes=20 * GB):
     assert 0 <= k < 16
     q = (1,) * 16 + (2048,)
