@@ -487,9 +487,13 @@ def run_trace(args, world, rank, local):
     out = torch.empty((budget, hq, a), dtype=bf, device=dev)
     maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
     max_seq = max(p + o - 1 for _, p, o in tr.requests)
-    sched = L.Scheduler(nb, bs, budget, min(budget, L.CB_MAX_REQS), wl.free_order(nb, tr.seed), maxblk)
-    for arr, p, o in tr.requests:
-        sched.add_request(arr, p, o)
+    def new_scheduler():
+        s = L.Scheduler(nb, bs, budget, min(budget, L.CB_MAX_REQS), wl.free_order(nb, tr.seed), maxblk)
+        for arr, p, o in tr.requests:
+            s.add_request(arr, p, o)
+        return s
+
+    sched = new_scheduler()
     ws = torch.empty(L.cb_paged_attention_workspace_size(min(budget, L.CB_MAX_REQS), budget, budget, max_seq, hq, hk,
                                                          a, bs), dtype=torch.uint8, device=dev)
     d_cu = torch.zeros(budget + 1, dtype=torch.int32, device=dev)
@@ -503,7 +507,7 @@ def run_trace(args, world, rank, local):
               sl=torch.zeros(budget, dtype=torch.int64).pin_memory(),
               ev=torch.cuda.Event()) for _ in range(2)]
     scale = 1.0 / math.sqrt(a)
-    stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0)
+    stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0, h2d=0, d2h=0)
 
     def one_step(i, host_io=None):
         m = sched.step()
@@ -537,6 +541,9 @@ def run_trace(args, world, rank, local):
             stats["launches"] += L.cb_last_launch_count()
             if host_io is not None:
                 host_io["out"][:t].copy_(out[:t], non_blocking=True)
+        if host_io is not None:
+            stats["h2d"] += nl * t * (hq + 2 * hk) * a * 2 + 4 * (2 * b + 1) + 4 * b * maxblk + 8 * t
+            stats["d2h"] += nl * t * hq * a * 2
         stats["tokens"] += t
         stats["steps"] += 1
         dec = int((q_lens == 1).sum())
@@ -579,26 +586,29 @@ def run_trace(args, world, rank, local):
     dev_s = e0.elapsed_time(e1) * 1e-3
     timed = dict(stats)
     elapsed = max_over_ranks(wall, world, dev)
-    # end to end: the following iterations take their new rows from pinned host
-    # memory and return every layer's output to the host
-    e2e = None
-    if not sched.done():
-        host_io = dict(q=[t.cpu().pin_memory() for t in qn], k=[t.cpu().pin_memory() for t in kn],
-                       v=[t.cpu().pin_memory() for t in vn], out=torch.empty_like(out, device="cpu").pin_memory())
-        for k in list(stats):
-            stats[k] = 0
-        n_e2e = min(50, args.steps)
-        te = time.perf_counter()
-        j = 0
-        while j < n_e2e and not sched.done():
-            one_step(args.warmup + args.steps + j, host_io)
-            j += 1
-        te = max_over_ranks(time.perf_counter() - te, world, dev)
-        t_e = stats["tokens"]
-        e2e = {"value": t_e * world / te if te > 0 else None, "unit": UNIT,
-               "h2d_bytes_per_step": int(nl * (budget * (hq + 2 * hk) * a * 2)) if j else 0,
-               "d2h_bytes_per_step": int(nl * budget * hq * a * 2) if j else 0, "steps": j,
-               "note": "h2d/d2h per step counted at the full 2048-token budget (upper bound)"}
+    # end to end: the same iterations again (a fresh scheduler from the trace's
+    # start), each layer's new rows copied from pinned host memory and each
+    # layer's output returned to the host, the host waiting for every iteration
+    host_io = dict(q=[t.cpu().pin_memory() for t in qn], k=[t.cpu().pin_memory() for t in kn],
+                   v=[t.cpu().pin_memory() for t in vn], out=torch.empty_like(out, device="cpu").pin_memory())
+    sched = new_scheduler()
+    for k in list(stats):
+        stats[k] = 0
+    for j in range(args.warmup):
+        one_step(j, host_io)
+    for k in list(stats):
+        stats[k] = 0
+    barrier(world)
+    te = time.perf_counter()
+    j = 0
+    while j < timed["steps"] + timed["idle"] and not sched.done():
+        one_step(args.warmup + j, host_io)
+        j += 1
+    te = max_over_ranks(time.perf_counter() - te, world, dev)
+    n_io = max(1, stats["steps"])
+    e2e = {"value": stats["tokens"] * world / te if te > 0 else None, "unit": UNIT,
+           "h2d_bytes_per_step": int(stats["h2d"] / n_io), "d2h_bytes_per_step": int(stats["d2h"] / n_io),
+           "steps": stats["steps"]}
     if rank != 0:
         return
     peaks = load_peaks()
