@@ -473,6 +473,7 @@ def run_trace(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream            # raw handle: the cheapest form for the per-layer calls
     tr = wl.trace(seed=args.seed + rank, pool_bytes=int(args.trace_pool_gb * wl.GB), n_layers=args.trace_layers)
     nl, hq, hk, a, bs, budget = tr.n_layers, tr.n_q_heads, tr.n_kv_heads, tr.head_dim, tr.block_size, tr.token_budget
     nb = tr.num_blocks
@@ -534,10 +535,10 @@ def run_trace(args, world, rank, local):
                 qn[layer][:t].copy_(host_io["q"][layer][:t], non_blocking=True)
                 kn[layer][:t].copy_(host_io["k"][layer][:t], non_blocking=True)
                 vn[layer][:t].copy_(host_io["v"][layer][:t], non_blocking=True)
-            L.cb_kv_append(kn[layer][:t], vn[layer][:t], d_sl[:t], kc[layer], vc[layer], stream)
+            L.cb_kv_append(kn[layer][:t], vn[layer][:t], d_sl[:t], kc[layer], vc[layer], sh)
             stats["launches"] += L.cb_last_launch_count()
             L.cb_paged_attention(qn[layer][:t], d_cu[:b + 1], d_ctx[:b], d_bt[:b], kc[layer], vc[layer], out[:t], scale,
-                                 ws, max_q, max_kv, stream)
+                                 ws, max_q, max_kv, sh)
             stats["launches"] += L.cb_last_launch_count()
             if host_io is not None:
                 host_io["out"][:t].copy_(out[:t], non_blocking=True)

@@ -75,32 +75,49 @@ def _check(fn, rc):
         raise CBError(fn, rc)
 
 
-def _stream(stream):
-    if stream is None:
+_torch = None
+
+
+def _t():
+    global _torch
+    if _torch is None:
         import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        _torch = torch
+    return _torch
+
+
+def _stream(stream):
+    """A stream handle: None = torch's current stream; an int is taken as the
+    raw cudaStream_t (the cheapest form for tight loops)."""
+    if stream is None:
+        return _t().cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def _dev(t, dtype, name, ndim=None):
-    import torch
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
-        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if ndim is not None and t.dim() != ndim:
+    """Raw device pointer of a contiguous CUDA tensor of the given dtype and rank."""
+    try:
+        ok = t.is_cuda and t.dtype is dtype and (ndim is None or t.dim() == ndim) and t.is_contiguous()
+    except AttributeError:
+        ok = False
+    if not ok:
+        torch = _t()
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def cb_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
     """k_new, v_new: bf16 [n_tokens, Hkv, A]; slot_mapping: int64 [n_tokens];
     k_cache, v_cache: bf16 [num_blocks, Hkv, block_size, A] (written in place)."""
-    import torch
+    torch = _t()
     bf = torch.bfloat16
     pk = _dev(k_new, bf, "k_new", 3)
     pv = _dev(v_new, bf, "v_new", 3)
@@ -127,7 +144,7 @@ def cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, o
     """q, out: bf16 [n_tokens, Hq, A]; cu_q_lens int32 [n_reqs+1]; ctx_lens int32 [n_reqs];
     block_tables int32 [n_reqs, max_blocks]; caches bf16 [num_blocks, Hkv, bs, A];
     workspace: uint8 CUDA tensor of at least cb_paged_attention_workspace_size bytes."""
-    import torch
+    torch = _t()
     bf = torch.bfloat16
     pq = _dev(q, bf, "q", 3)
     po = _dev(out, bf, "out", 3)
@@ -160,7 +177,7 @@ def cb_paged_attention_noalloc(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_
     fixed device array (CB_NOALLOC_SCRATCH_BYTES); steps that need more are
     rejected (CBError, CB_EWORKSPACE).  Calls that overlap on the GPU share that
     array and race."""
-    import torch
+    torch = _t()
     bf = torch.bfloat16
     pq = _dev(q, bf, "q", 3)
     po = _dev(out, bf, "out", 3)

@@ -3,6 +3,7 @@
 // error word).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/cbattn.h"
@@ -241,12 +242,13 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
   if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
   cudaError_t e;
   if (max_q_len == 1 && block_tiles) {
-    e = launch_decode_tcb(p, maps[3], maps[4], maps[5], group, di.n_sms, s);
+    e = launch_decode_tcb(p, maps[3], maps[4], maps[5], group, std::min(di.n_sms, kMaxDecodeGrid), s);
   } else if (max_q_len == 1) {
     e = launch_decode(p, maps[0], maps[1], head_dim, group, di.n_sms, s);
   } else {
     if (!block_tiles) maps[3] = maps[4] = maps[5] = maps[0];   // unused by the kernel
-    e = launch_mixed(p, maps, block_tiles, head_dim, group, di.n_sms, s);
+    e = launch_mixed(p, maps, block_tiles, head_dim, group, block_tiles ? std::min(di.n_sms, kMaxDecodeGrid) : di.n_sms,
+                     s);
   }
   if (e != cudaSuccess) return CB_ECUDA;
   g_last_launches = 1;

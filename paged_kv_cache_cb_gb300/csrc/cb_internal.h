@@ -22,6 +22,7 @@ constexpr int kTileM = 128;        // query rows per tensor-core tile
 constexpr int kTileN = 128;        // keys per tensor-core tile
 constexpr int kMaxReqs = 2048;     // requests per step (plan arrays live in shared memory)
 constexpr int kMaxSplitBlocks = 32;  // decode split size limit (one warp-wide table load)
+constexpr int kMaxDecodeGrid = 160;  // CTAs of the block-tile decode launches (at most one per SM)
 
 // Everything a step's attention kernels read besides the tensor maps.
 struct StepParams {
