@@ -227,7 +227,7 @@ struct MmaIssuer {
     const int st = kj & 1;
     if (!mbar_ready(&C.k_full[st], (kj >> 1) & 1)) return false;
     tc_fence_after();
-    const uint64_t q0 = qd[SIDE], k0 = kd[st];
+    const uint64_t q0 = qd[SIDE], k0 = st ? kd[1] : kd[0];   // (a select: an indexed array would live in local memory)
 #pragma unroll
     for (int ks = 0; ks < A / 16; ++ks) {
       const uint64_t off = ((ks >> 2) * PrefillTiles<A>::kHalfBytes + (ks & 3) * 32) >> 4;
@@ -247,7 +247,7 @@ struct MmaIssuer {
     if (j == 0 && !mbar_ready(&C.o_free[SIDE], (it & 1) ^ 1)) return false;
     ++pc;
     tc_fence_after();
-    const uint64_t v0 = vd[st];
+    const uint64_t v0 = st ? vd[1] : vd[0];
     const uint32_t p_t = tmem + SIDE * 128;
     const uint32_t o_t = tmem + 256 + SIDE * A;
 #pragma unroll
