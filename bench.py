@@ -659,7 +659,8 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.workload == "trace":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "trace workload: the reference arm times single steps"}))
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "trace workload: the reference arm times single steps"}))
             return
         run_trace(args, world, rank, local)
         if world > 1:
