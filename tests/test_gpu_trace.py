@@ -80,3 +80,81 @@ def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
     assert checked > 20
     if num_blocks == 16:
         assert preempted > 0, "the tight pool is meant to exercise preemption"
+
+
+def test_full_size_trace_sampled():
+    """The full continuous-batching trace (256 requests, 32 layers of GQA 32/8 x
+    128, FCFS with a 2048-token budget, 60 GB pool) through the library; sampled
+    (iteration, layer, request) outputs against the oracle.  Each layer's new
+    rows come from one fixed seeded buffer indexed by the token's place in its
+    step, so a map (request, position) -> that index rebuilds any request's keys
+    and values on the host."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = L()
+    tr = wl.trace(seed=0)
+    nl, hq, hk, a, bs, budget, nb = tr.n_layers, tr.n_q_heads, tr.n_kv_heads, tr.head_dim, tr.block_size, \
+        tr.token_budget, tr.num_blocks
+    dev = torch.device("cuda")
+    kc = [torch.zeros((nb, hk, bs, a), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+    vc = [torch.zeros_like(kc[0]) for _ in range(nl)]
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    qn = [torch.randn((budget, hq, a), generator=g, device=dev, dtype=torch.bfloat16) for _ in range(nl)]
+    kn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=torch.bfloat16) for _ in range(nl)]
+    vn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=torch.bfloat16) for _ in range(nl)]
+    out = torch.empty((budget, hq, a), dtype=torch.bfloat16, device=dev)
+    maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
+    max_seq = max(p + o - 1 for _, p, o in tr.requests)
+    sched = lib.Scheduler(nb, bs, budget, min(budget, lib.CB_MAX_REQS), wl.free_order(nb, tr.seed), maxblk)
+    for arr, p, o in tr.requests:
+        sched.add_request(arr, p, o)
+    ws = torch.empty(lib.cb_paged_attention_workspace_size(min(budget, lib.CB_MAX_REQS), budget, budget, max_seq, hq,
+                                                           hk, a, bs), dtype=torch.uint8, device=dev)
+    check_layers = (0, 13, nl - 1)
+    host = {l: (kn[l].double().cpu().numpy(), vn[l].double().cpu().numpy()) for l in check_layers}
+    tok_of = {}                    # (rid, pos) -> index of the row in its step's new-row buffers
+    rng = np.random.default_rng(11)
+    steps = checked = 0
+    while not sched.done():
+        m = sched.step()
+        steps += 1
+        b = len(m["req_ids"])
+        if b == 0:
+            continue
+        t = int(m["cu_q_lens"][-1])
+        cu = torch.from_numpy(m["cu_q_lens"]).to(dev)
+        ctx = torch.from_numpy(m["ctx_lens"]).to(dev)
+        bt = torch.from_numpy(np.ascontiguousarray(m["block_tables"])).to(dev)
+        sl = torch.from_numpy(m["slot_mapping"]).to(dev)
+        q_lens, ctx_lens, rids = m["q_lens"].tolist(), m["ctx_lens"].tolist(), m["req_ids"].tolist()
+        max_q, max_kv = max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens))
+        tok = 0
+        for rid, n, c in zip(rids, q_lens, ctx_lens):
+            for i in range(n):
+                tok_of[(rid, c + i)] = tok
+                tok += 1
+        check = steps % 150 == 1 or (max_q > 1 and steps % 37 == 0)
+        for layer in range(nl):
+            lib.cb_kv_append(kn[layer][:t], vn[layer][:t], sl, kc[layer], vc[layer])
+            lib.cb_paged_attention(qn[layer][:t], cu, ctx, bt, kc[layer], vc[layer], out[:t], 1 / math.sqrt(a), ws,
+                                   max_q, max_kv)
+            if check and layer in check_layers:
+                got = out[:t].double().cpu().numpy()
+                qd = qn[layer][:t].double().cpu().numpy()
+                kd, vd = host[layer]
+                cu_h = m["cu_q_lens"]
+                picks = sorted(set([0, b - 1] + rng.choice(b, size=min(2, b), replace=False).tolist()))
+                for j in picks:
+                    rid, n, c = rids[j], q_lens[j], ctx_lens[j]
+                    idx = [tok_of[(rid, p)] for p in range(c + n)]
+                    # a long chunk: its first and last rows and a few in between
+                    rows = sorted(set([0, n - 1] + rng.choice(n, size=min(n, 4), replace=False).tolist()))
+                    ref = oa.attention_rows(qd[cu_h[j] + np.array(rows)], kd[idx], vd[idx], [c + i for i in rows],
+                                            1 / math.sqrt(a), hq, hk)
+                    assert_close(got[cu_h[j] + np.array(rows)], ref, f"step {steps} layer {layer} request {rid}")
+                    checked += 1
+        assert lib.cb_last_error() == 0, f"step {steps}"
+    assert steps > 1000 and checked > 60
+    del kc, vc
+    torch.cuda.empty_cache()
