@@ -59,7 +59,10 @@ def _no_alloc(m):
     wl.tiny(),                                                              # mixed: decodes, a chunk, a prefill
     wl.random_step(21, n_reqs=12, max_ctx=2500, max_q=1, n_q_heads=8, n_kv_heads=2, head_dim=128, p_decode=1.0),
     wl.random_step(22, n_reqs=9, max_ctx=900, max_q=200, n_q_heads=16, n_kv_heads=4, head_dim=128),
-], ids=lambda s: s.name)
+    # 8 KV heads: the block-tile decode (its own launch, and the mixed launch's decode phase)
+    wl.random_step(23, n_reqs=12, max_ctx=2500, max_q=1, n_q_heads=32, n_kv_heads=8, head_dim=128, p_decode=1.0),
+    wl.random_step(24, n_reqs=9, max_ctx=900, max_q=200, n_q_heads=32, n_kv_heads=8, head_dim=128),
+], ids=lambda s: f"{s.name}_h{s.n_q_heads}_{s.n_kv_heads}")
 def test_no_alloc_matches_workspace_entry_point_twice(shape):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
