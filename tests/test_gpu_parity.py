@@ -226,6 +226,46 @@ def test_empty_batch_and_zero_length_requests():
     assert lib.cb_last_launch_count() == 0
 
 
+@pytest.mark.parametrize("q_lens,ctx_lens", [((0, 1, 0, 1, 0), (10, 50, 0, 300, 7)),
+                                             ((0, 3, 0, 1, 40, 0), (10, 5, 0, 300, 100, 20))],
+                         ids=["decode_only", "mixed"])
+def test_zero_length_requests_eight_kv_heads(q_lens, ctx_lens):
+    """Requests with no new token between decodes and chunks, 8 KV heads: the
+    block-tile decode must skip them when it walks the requests' blocks."""
+    blocks = sum(-(-(c + q) // 16) for c, q in zip(ctx_lens, q_lens)) + 8
+    _parity(wl.StepShape("zero_q_8kv", 32, 8, 128, 16, blocks, q_lens=q_lens, ctx_lens=ctx_lens, seed=3))
+
+
+def test_bad_block_id_in_mixed_eight_kv_heads_is_reported():
+    shape = wl.StepShape("bad_mixed_8kv", 32, 8, 128, 16, 200, q_lens=(1, 1, 60, 1), ctx_lens=(300, 40, 100, 250),
+                         seed=4)
+    inp = wl.step_inputs_cpu(shape)
+    bad = inp["block_tables"].copy()
+    bad[1, 1] = shape.num_blocks + 3          # a decode reads it
+    lib = L()
+    out, _, _, status = device_step(shape, inp, check=False, attn_tables=bad)
+    assert status == lib.CB_EDEVICE
+    ref = oracle_step(shape, inp)
+    cu = np.concatenate([[0], np.cumsum(shape.q_lens)])
+    for r in (0, 2, 3):
+        assert_close(f64(out[cu[r]:cu[r + 1]]), ref[cu[r]:cu[r + 1]], f"request {r}")
+
+
+def test_max_requests_mixed_eight_kv_heads():
+    """CB_MAX_REQS requests in one mixed launch with 8 KV heads: 2040 decodes
+    with short contexts and 8 short prefill chunks."""
+    lib = L()
+    n = lib.CB_MAX_REQS
+    rng = np.random.default_rng(5)
+    ctx = [int(c) for c in rng.integers(0, 40, size=n)]
+    q = [1] * n
+    for r in range(0, n, n // 8):
+        q[r] = 20
+    shape = wl.StepShape("max_reqs_mixed_8kv", 32, 8, 128, 16, sum(-(-(c + k) // 16) for c, k in zip(ctx, q)) + 4,
+                         q_lens=tuple(q), ctx_lens=tuple(ctx), seed=10)
+    _parity(shape)
+
+
 def test_block_and_tile_boundaries():
     """Lengths at exact multiples of the block (16) and tile (128) sizes and one past."""
     shape = wl.StepShape("bounds", 8, 2, 128, 16, 300, q_lens=(1, 1, 128, 129, 16, 1),
