@@ -126,6 +126,33 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
                                          int n_q_heads, int n_kv_heads, int head_dim, int block_size);
 
+/* ---------------------------------------------------------------- append + attention
+ * One whole step of a layer ([CB] Chunked prefill: the chunk's K/V states are
+ * stored, then its queries attend to the cached prefix and to themselves):
+ * the same result as cb_kv_append(k_new, v_new, slot_mapping, n_tokens, ...)
+ * followed by cb_paged_attention(q, ...) on `stream`, with the arguments of
+ * both (n_tokens, the cache, num_blocks and the shape are shared; k_cache and
+ * v_cache are written).  Token t's new rows go to slot_mapping[t] before any
+ * request reads the cache, so every new token attends to its own key.
+ * Where the attention launch is cooperative (8 KV heads, head_dim 128, G >= 2)
+ * its CTAs store the rows themselves and meet at a grid-wide counter in the
+ * workspace before the first cache read: one kernel launch for the step.
+ * Other shapes run the two kernels back to back.
+ *  k_new, v_new   device, bf16 [n_tokens][n_kv_heads][head_dim], 16-byte aligned
+ *  slot_mapping   device, int64 [n_tokens]; < 0 skips the token
+ *  workspace      cb_paged_attention_workspace_size(...) bytes, as for
+ *                 cb_paged_attention
+ * Errors: those of the two calls; a slot >= num_blocks * block_size is skipped
+ * and reported like a bad block id (cb_last_error -> CB_EDEVICE).
+ */
+int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                 const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                                 const int32_t* block_tables, int max_blocks_per_seq, int n_reqs,
+                                 int n_tokens, int max_q_len, int max_kv_len, void* k_cache,
+                                 void* v_cache, int num_blocks, void* out, float scale, int n_q_heads,
+                                 int n_kv_heads, int head_dim, int block_size, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- no-allocation variant
  * The pages have no counterpart: this exists for callers that cannot allocate
  * device memory when they run a step -- hosts whose device memory is owned by

@@ -28,6 +28,9 @@ SIGNATURES = [
     ("cb_paged_attention", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                     _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     ("cb_paged_attention_workspace_size", _c_size, [_c_int] * 8),
+    ("cb_kv_append_paged_attention", _c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                              _c_int, _vp, _vp, _c_int, _vp, _c_float, _c_int, _c_int, _c_int,
+                                              _c_int, _vp, _c_size, _vp]),
     ("cb_paged_attention_noalloc", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                                             _c_int, _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp]),
     ("cb_last_error", _c_int, [_vp]),
@@ -165,6 +168,39 @@ def cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, o
                                   int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs, pw,
                                   workspace.numel(), _stream(stream))
     _check("cb_paged_attention", rc)
+
+
+def cb_kv_append_paged_attention(k_new, v_new, slot_mapping, q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache,
+                                 out, scale, workspace, max_q_len, max_kv_len, stream=None):
+    """cb_kv_append of the step's new rows, then cb_paged_attention, as one call
+    (one kernel launch where the attention launch is cooperative).  Arguments as
+    for those two; k_new, v_new: bf16 [n_tokens, Hkv, A] with n_tokens = q's."""
+    torch = _t()
+    bf = torch.bfloat16
+    pk = _dev(k_new, bf, "k_new", 3)
+    pv = _dev(v_new, bf, "v_new", 3)
+    ps = _dev(slot_mapping, torch.int64, "slot_mapping", 1)
+    pq = _dev(q, bf, "q", 3)
+    po = _dev(out, bf, "out", 3)
+    pcu = _dev(cu_q_lens, torch.int32, "cu_q_lens", 1)
+    pctx = _dev(ctx_lens, torch.int32, "ctx_lens", 1)
+    pbt = _dev(block_tables, torch.int32, "block_tables", 2)
+    ck = _dev(k_cache, bf, "k_cache", 4)
+    cv = _dev(v_cache, bf, "v_cache", 4)
+    pw = _dev(workspace, torch.uint8, "workspace", 1)
+    n_tok, hq, a = q.shape
+    n_reqs = ctx_lens.numel()
+    if out.shape != q.shape or cu_q_lens.numel() != n_reqs + 1 or block_tables.shape[0] != n_reqs:
+        raise ValueError("shape mismatch")
+    nb, hk, bs, a2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or a2 != a:
+        raise ValueError("cache shape mismatch")
+    if k_new.shape != (n_tok, hk, a) or v_new.shape != k_new.shape or slot_mapping.numel() != n_tok:
+        raise ValueError("new rows must be [n_tokens, Hkv, A] with one slot per token")
+    rc = lib().cb_kv_append_paged_attention(pk, pv, ps, pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok,
+                                            int(max_q_len), int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk,
+                                            a, bs, pw, workspace.numel(), _stream(stream))
+    _check("cb_kv_append_paged_attention", rc)
 
 
 CB_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024

@@ -172,11 +172,25 @@ size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len
   return workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks).total;
 }
 
-int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
-                       int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
-                       const void* k_cache, const void* v_cache, int num_blocks, void* out, float scale,
-                       int n_q_heads, int n_kv_heads, int head_dim, int block_size, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The step's new K/V rows, for the entry point that stores them too.
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+};
+
+// Attention step, optionally preceded by the append of the step's new rows
+// (app != nullptr): inside the attention launch where it is cooperative (the
+// block-tile paths), else as a cb_kv_append launch before it.
+int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                   const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len,
+                   int max_kv_len, const void* k_cache, const void* v_cache, int num_blocks, void* out, float scale,
+                   int n_q_heads, int n_kv_heads, int head_dim, int block_size, void* workspace,
+                   size_t workspace_bytes, void* stream) {
   if (!shape_ok(n_q_heads, n_kv_heads, head_dim, block_size)) return CB_EINVAL;
   if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
       max_blocks_per_seq < 1 || num_blocks <= 0 || !(scale > 0.f) || max_q_len > max_kv_len)
@@ -188,6 +202,8 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
   }
   if (!q || !cu_q_lens || !ctx_lens || !block_tables || !k_cache || !v_cache || !out || !workspace) return CB_EINVAL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
+    return CB_EINVAL;
+  if (app && (!app->k_new || !app->v_new || !app->slots || !aligned16(app->k_new) || !aligned16(app->v_new)))
     return CB_EINVAL;
   const WorkspaceLayout L = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8);
   if (workspace_bytes < L.total) return CB_EWORKSPACE;
@@ -238,21 +254,63 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
         !encode_q_map(&maps[5], q, n_tokens, n_q_heads, head_dim, n_q_heads, 1))
       return CB_ECUDA;
   }
+  // the append goes into the launch where that launch is cooperative
+  AppendParams ap{};
+  int launches = 1;
+  if (app && block_tiles) {
+    ap.k_new = static_cast<const uint4*>(app->k_new);
+    ap.v_new = static_cast<const uint4*>(app->v_new);
+    ap.slots = app->slots;
+    ap.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+    ap.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+    ap.n_tokens = n_tokens;
+  } else if (app) {
+    if (launch_kv_append(app->k_new, app->v_new, app->slots, n_tokens, const_cast<void*>(k_cache),
+                         const_cast<void*>(v_cache), num_blocks, n_kv_heads, head_dim, di.err, s) != cudaSuccess)
+      return CB_ECUDA;
+    launches = 2;
+  }
   // split arrival counters and the work queue start at zero every call
   if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
   cudaError_t e;
   if (max_q_len == 1 && block_tiles) {
-    e = launch_decode_tcb(p, maps[3], maps[4], maps[5], group, std::min(di.n_sms, kMaxDecodeGrid), s);
+    e = launch_decode_tcb(p, ap, maps[3], maps[4], maps[5], group, std::min(di.n_sms, kMaxDecodeGrid), s);
   } else if (max_q_len == 1) {
     e = launch_decode(p, maps[0], maps[1], head_dim, group, di.n_sms, s);
   } else {
     if (!block_tiles) maps[3] = maps[4] = maps[5] = maps[0];   // unused by the kernel
-    e = launch_mixed(p, maps, block_tiles, head_dim, group, block_tiles ? std::min(di.n_sms, kMaxDecodeGrid) : di.n_sms,
+    e = launch_mixed(p, ap, maps, block_tiles, head_dim, group, block_tiles ? std::min(di.n_sms, kMaxDecodeGrid) : di.n_sms,
                      s);
   }
   if (e != cudaSuccess) return CB_ECUDA;
-  g_last_launches = 1;
+  g_last_launches = launches;
   return CB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
+                       int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
+                       const void* k_cache, const void* v_cache, int num_blocks, void* out, float scale,
+                       int n_q_heads, int n_kv_heads, int head_dim, int block_size, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attention_step(nullptr, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens,
+                        max_q_len, max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads,
+                        head_dim, block_size, workspace, workspace_bytes, stream);
+}
+
+int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+                                 const int32_t* cu_q_lens, const int32_t* ctx_lens, const int32_t* block_tables,
+                                 int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
+                                 void* k_cache, void* v_cache, int num_blocks, void* out, float scale, int n_q_heads,
+                                 int n_kv_heads, int head_dim, int block_size, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  const AppendArgs app{k_new, v_new, slot_mapping};
+  return attention_step(&app, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens, max_q_len,
+                        max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads, head_dim,
+                        block_size, workspace, workspace_bytes, stream);
 }
 
 int cb_last_error(void* stream) {

@@ -15,27 +15,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                         int64_t n_slots, int n_kv_heads, int chunks_per_row,
                                                         unsigned int* __restrict__ err) {
-  const int64_t per_token = (int64_t)n_kv_heads * chunks_per_row;   // 16-byte pieces per token (one of K/V)
-  const int64_t total = (int64_t)n_tokens * per_token;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / per_token;
-    const int64_t rem = i - t * per_token;       // = g * chunks_per_row + c
-    const int64_t g = rem / chunks_per_row;
-    const int64_t c = rem - g * chunks_per_row;
-    const int64_t slot = __ldg(slots + t);
-    if (slot < 0) continue;                      // "do not write this token"
-    if (slot >= n_slots) {
-      set_error(err, CB_DEVERR_BADSLOT);
-      continue;
-    }
-    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-    // cache index of (blk, g, off, c) in 16-byte units
-    const int64_t dst = ((blk * n_kv_heads + g) * kBlockSize + off) * chunks_per_row + c;
-    const uint4 kv = __ldg(k_new + i);
-    const uint4 vv = __ldg(v_new + i);
-    k_cache[dst] = kv;
-    v_cache[dst] = vv;
-  }
+  append_pieces(k_new, v_new, slots, n_tokens, k_cache, v_cache, n_slots, n_kv_heads, chunks_per_row, err,
+                blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t* slots, int n_tokens, void* k_cache,

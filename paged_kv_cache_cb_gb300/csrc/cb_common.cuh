@@ -115,6 +115,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// The same for global memory: generic stores that a TMA load will read.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
@@ -357,6 +361,41 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- KV append
+// Slot-mapped append ([CB] Chunked prefill: the chunk's K/V states are stored;
+// [SM] PagedAttention: the slot picks block slot / bs and offset slot % bs):
+// piece i of the new rows, i = (t * Hkv + g) * chunks_per_row + c, is 16 bytes
+// of token t's row for KV head g and lands at cache row (blk, g, off).  This
+// thread copies pieces i0, i0 + stride, ...; consecutive threads take
+// consecutive pieces of one row, so loads and stores are both coalesced.
+// Slot < 0 skips the token; slot >= n_slots skips it and sets CB_DEVERR_BADSLOT.
+__device__ __forceinline__ void append_pieces(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                              const int64_t* __restrict__ slots, int n_tokens,
+                                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                              int64_t n_slots, int n_kv_heads, int chunks_per_row,
+                                              unsigned int* err, int64_t i0, int64_t stride) {
+  const int64_t per_token = (int64_t)n_kv_heads * chunks_per_row;
+  const int64_t total = (int64_t)n_tokens * per_token;
+  for (int64_t i = i0; i < total; i += stride) {
+    const int64_t t = i / per_token;
+    const int64_t rem = i - t * per_token;       // = g * chunks_per_row + c
+    const int64_t g = rem / chunks_per_row;
+    const int64_t c = rem - g * chunks_per_row;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= n_slots) {
+      set_error(err, CB_DEVERR_BADSLOT);
+      continue;
+    }
+    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+    const int64_t dst = ((blk * n_kv_heads + g) * kBlockSize + off) * chunks_per_row + c;
+    const uint4 kv = __ldg(k_new + i);
+    const uint4 vv = __ldg(v_new + i);
+    k_cache[dst] = kv;
+    v_cache[dst] = vv;
+  }
 }
 
 }  // namespace cb

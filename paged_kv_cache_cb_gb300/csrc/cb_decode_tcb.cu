@@ -12,7 +12,7 @@ constexpr int kSmemLimit = 232448;
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_tcb_kernel(const StepParams P, const __grid_constant__ CUtensorMap kmap,
+    decode_tcb_kernel(const StepParams P, const AppendParams Ap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -36,9 +36,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
     tc_fence_before();
   }
+  append_phase(P, Ap);             // the step's new rows, when this launch stores them
   for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) bpre[r] = decode_blocks(P, r, false);
   __syncthreads();
   finish_plan<G>(P, C, bpre, slot);
+  append_wait(P, Ap);
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   run_pipeline<G>(P, &kmap, &vmap, &qmap, T, C, bpre, slot, tmem);
@@ -60,8 +62,8 @@ static_assert(smem_bytes<4>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 static_assert(smem_bytes<8>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 
 template <int G>
-cudaError_t launch_t(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                     int n_sms, cudaStream_t stream) {
+cudaError_t launch_t(const StepParams& p, const AppendParams& ap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     const CUtensorMap& qmap, int n_sms, cudaStream_t stream) {
   const size_t smem = smem_bytes<G>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
   static bool attr_set = false;
@@ -73,7 +75,8 @@ cudaError_t launch_t(const StepParams& p, const CUtensorMap& kmap, const CUtenso
   }
   // cooperative: the merge phase waits for every CTA
   StepParams pc = p;
-  void* args[] = {&pc, const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap),
+  AppendParams apc = ap;
+  void* args[] = {&pc, &apc, const_cast<CUtensorMap*>(&kmap), const_cast<CUtensorMap*>(&vmap),
                   const_cast<CUtensorMap*>(&qmap)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(decode_tcb_kernel<G>), dim3(n_sms), dim3(kThreads),
                                      args, smem, stream);
@@ -81,12 +84,13 @@ cudaError_t launch_t(const StepParams& p, const CUtensorMap& kmap, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_decode_tcb(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, int group, int n_sms, cudaStream_t stream) {
+cudaError_t launch_decode_tcb(const StepParams& p, const AppendParams& ap, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const CUtensorMap& qmap, int group, int n_sms,
+                              cudaStream_t stream) {
   switch (group) {
-    case 2: return launch_t<2>(p, kmap, vmap, qmap, n_sms, stream);
-    case 4: return launch_t<4>(p, kmap, vmap, qmap, n_sms, stream);
-    case 8: return launch_t<8>(p, kmap, vmap, qmap, n_sms, stream);
+    case 2: return launch_t<2>(p, ap, kmap, vmap, qmap, n_sms, stream);
+    case 4: return launch_t<4>(p, ap, kmap, vmap, qmap, n_sms, stream);
+    case 8: return launch_t<8>(p, ap, kmap, vmap, qmap, n_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -775,6 +775,45 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
   return v;
 }
 
+// ---------------------------------------------------------------- fused KV append (all threads)
+// A launch given the step's new K/V rows (Ap.n_tokens > 0) stores them before
+// anything reads the cache: every thread of the grid copies its share of the
+// 16-byte pieces (append_pieces), then the CTA arrives on the grid-wide counter
+// P.queue[2].  The launch is cooperative, so all CTAs are resident and the
+// counter reaches gridDim.x.  The stores are made visible to the async proxy
+// (the TMA loads of the producers) on both sides of the counter.  Not inlined:
+// the copy loop's registers stay out of the pipeline's allocation.
+static __device__ __noinline__ void append_store(const AppendParams& Ap, int64_t n_slots, unsigned int* err) {
+  append_pieces(Ap.k_new, Ap.v_new, Ap.slots, Ap.n_tokens, Ap.k_cache, Ap.v_cache, n_slots, kHkv, 16, err,
+                blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+  fence_proxy_async_global();
+  __threadfence();
+}
+__device__ __forceinline__ void append_phase(const StepParams& P, const AppendParams& Ap) {
+  if (Ap.n_tokens == 0) return;
+  append_store(Ap, (int64_t)P.num_blocks * kBlockSize, P.err);
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(P.queue + 2, 1);
+}
+// Bounded wait until every CTA has arrived after its append stores; a time-out
+// records CB_DEVERR_TIMEOUT and goes on (the step's result is then unreliable,
+// and the host is told).  All threads of the CTA call it.
+__device__ __forceinline__ void append_wait(const StepParams& P, const AppendParams& Ap) {
+  if (Ap.n_tokens == 0) return;
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(P.queue + 2) < gridDim.x) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(P.err, CB_DEVERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
+  fence_proxy_async_global();
+}
+
 // After the pipeline: a grid-wide barrier (the launch is cooperative, so every
 // CTA is resident; the wait is bounded), then every warp of the grid merges one
 // (request, q head) of the requests cut into several splits at a time, by

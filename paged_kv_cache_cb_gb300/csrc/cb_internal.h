@@ -49,6 +49,19 @@ struct StepParams {
   unsigned int* err;            // device error word
 };
 
+// The step's new K/V rows when the block-tile launches store them themselves
+// (n_tokens == 0: they do not): the launch first stores token t's rows at
+// slots[t], then waits for every CTA's stores (StepParams::queue[2]) before its
+// first cache read.
+struct AppendParams {
+  const uint4* k_new;           // bf16 [n_tokens][Hkv][A] as 16-byte pieces
+  const uint4* v_new;
+  const int64_t* slots;         // [n_tokens]
+  uint4* k_cache;               // the caches that the tensor maps read
+  uint4* v_cache;
+  int n_tokens;
+};
+
 // Workspace carving (byte offsets), shared by the size query and the launcher.
 struct WorkspaceLayout {
   size_t counters, queue, part_ml, part_acc, total;
@@ -68,13 +81,14 @@ cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CU
 // must have 128-row boxes and the q map a box of one token's Hq heads.  It
 // cuts the work into equal pieces itself (p.split_blocks is not used); the
 // partial buffers must hold n_reqs * (ceil(max blocks / 8) + 1) splits.
-cudaError_t launch_decode_tcb(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, int group, int n_sms, cudaStream_t stream);
+cudaError_t launch_decode_tcb(const StepParams& p, const AppendParams& ap, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const CUtensorMap& qmap, int group, int n_sms,
+                              cudaStream_t stream);
 // Mixed prefill + decode step.  maps: K, V with 16-row boxes, the prefill q
 // map, then (block_tiles: the block-tile decode phase) K, V with 128-row boxes
 // and the decode q map.
-cudaError_t launch_mixed(const StepParams& p, const CUtensorMap* maps, bool block_tiles, int head_dim, int group,
-                         int n_sms, cudaStream_t stream);
+cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, bool block_tiles,
+                         int head_dim, int group, int n_sms, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
 cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream);
 

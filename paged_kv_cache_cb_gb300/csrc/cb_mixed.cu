@@ -524,7 +524,8 @@ constexpr size_t mixed_smem(int n_reqs) {
 
 template <int A, int G, bool BT>
 __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
-    mixed_kernel(const StepParams P, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    mixed_kernel(const StepParams P, const AppendParams Ap, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap,
                  const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_b,
                  const __grid_constant__ CUtensorMap vmap_b, const __grid_constant__ CUtensorMap qmap_d) {
   constexpr int TOK = kTileM / G;
@@ -576,6 +577,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
   if constexpr (BT) {
     // prefill items per request and decode blocks per request, both in request order
     tcb::Ctl<G>& C2 = *reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl));
+    tcb::append_phase(P, Ap);      // the step's new rows, when this launch stores them
     for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) {
       pre[r] = request_work(P, r, 2 * TOK, true).pre_items;
       a1[r] = tcb::decode_blocks(P, r, true);
@@ -583,6 +585,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     __syncthreads();
     tcb::block_scan_excl(pre, P.n_reqs, C2.scratch);
     tcb::finish_plan<G>(P, C2, a1, a2);
+    tcb::append_wait(P, Ap);       // before the first TMA load of the cache
   } else {
     build_plan(P, 2 * TOK, a0, a1, a2, C.scratch);   // ends with __syncthreads()
   }
@@ -631,9 +634,11 @@ static_assert(mixed_smem<128, 4, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared 
 static_assert(mixed_smem<128, 8, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 
 template <int A, int G, bool BT>
-cudaError_t launch_mixed_t(const StepParams& p, const CUtensorMap* maps, int n_sms, cudaStream_t stream) {
+cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, int n_sms,
+                           cudaStream_t stream) {
   const size_t smem = mixed_smem<A, G, BT>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
+  if (!BT && ap.n_tokens != 0) return cudaErrorInvalidValue;   // only the cooperative launch stores rows
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -643,25 +648,26 @@ cudaError_t launch_mixed_t(const StepParams& p, const CUtensorMap* maps, int n_s
   }
   if constexpr (BT) {   // cooperative: the decode merge phase waits for every CTA
     StepParams pc = p;
-    void* args[] = {&pc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
+    AppendParams apc = ap;
+    void* args[] = {&pc, &apc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
                     const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
                     const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5])};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), dim3(n_sms),
                                        dim3(tcb::kThreads), args, smem, stream);
   } else {
-    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                   maps[5]);
+    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, ap, maps[0], maps[1], maps[2], maps[3],
+                                                                   maps[4], maps[5]);
     return cudaGetLastError();
   }
 }
 
 }  // namespace
 
-cudaError_t launch_mixed(const StepParams& p, const CUtensorMap* maps, bool block_tiles, int head_dim, int group,
-                         int n_sms, cudaStream_t stream) {
+cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, bool block_tiles,
+                         int head_dim, int group, int n_sms, cudaStream_t stream) {
 #define CB_MIX_CASE(A_, G_, BT_)                  \
   if (head_dim == A_ && group == G_ && block_tiles == BT_) \
-    return launch_mixed_t<A_, G_, BT_>(p, maps, n_sms, stream);
+    return launch_mixed_t<A_, G_, BT_>(p, ap, maps, n_sms, stream);
   CB_MIX_CASE(128, 2, true)
   CB_MIX_CASE(128, 4, true)
   CB_MIX_CASE(128, 8, true)

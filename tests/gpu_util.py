@@ -26,28 +26,36 @@ def cu_of(q_lens):
     return np.concatenate([[0], np.cumsum(np.asarray(q_lens, np.int64))]).astype(np.int32)
 
 
-def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True, attn_tables=None):
+def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True, attn_tables=None, fused=False,
+                slots=None):
     """Append the step's new K/V and run attention; returns (out, k_cache, v_cache, status).
     ``attn_tables`` replaces the block tables that attention reads (the append
-    still uses the slots of ``inp["block_tables"]``)."""
+    still uses the slots of ``inp["block_tables"]``, or ``slots`` if given).
+    ``fused``: one cb_kv_append_paged_attention call instead of the two."""
     lib = L()
     scale = scale if scale is not None else 1.0 / math.sqrt(shape.head_dim)
-    slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, inp["block_tables"], shape.block_size)
+    if slots is None:
+        slots = lib.cb_build_slot_mapping(shape.q_lens, shape.ctx_lens, inp["block_tables"], shape.block_size)
     bt = inp["block_tables"] if attn_tables is None else attn_tables
     k_cache = inp["k_pool"].to(dev).clone() if inp["k_pool"].device.type == "cpu" else inp["k_pool"]
     v_cache = inp["v_pool"].to(dev).clone() if inp["v_pool"].device.type == "cpu" else inp["v_pool"]
     q = inp["q"].to(dev)
     k_new, v_new = inp["k_new"].to(dev), inp["v_new"].to(dev)
-    lib.cb_kv_append(k_new, v_new, torch.from_numpy(slots).to(dev), k_cache, v_cache)
+    d_slots = torch.from_numpy(np.asarray(slots, np.int64)).to(dev)
+    if not fused:
+        lib.cb_kv_append(k_new, v_new, d_slots, k_cache, v_cache)
     kv = [c + n for c, n in zip(shape.ctx_lens, shape.q_lens)]
     max_q, max_kv = max(max(shape.q_lens), 1), max(max(kv), 1)
     wsb = lib.cb_paged_attention_workspace_size(shape.n_reqs, shape.n_tokens, max_q, max_kv, shape.n_q_heads,
                                                 shape.n_kv_heads, shape.head_dim, shape.block_size)
     ws = torch.empty(wsb + ws_extra, dtype=torch.uint8, device=dev)
     out = torch.full_like(q, float("nan"))
-    lib.cb_paged_attention(q, torch.from_numpy(cu_of(shape.q_lens)).to(dev),
-                           torch.tensor(shape.ctx_lens, dtype=torch.int32, device=dev),
-                           torch.from_numpy(bt).to(dev), k_cache, v_cache, out, scale, ws, max_q, max_kv)
+    meta = (q, torch.from_numpy(cu_of(shape.q_lens)).to(dev), torch.tensor(shape.ctx_lens, dtype=torch.int32, device=dev),
+            torch.from_numpy(bt).to(dev))
+    if fused:
+        lib.cb_kv_append_paged_attention(k_new, v_new, d_slots, *meta, k_cache, v_cache, out, scale, ws, max_q, max_kv)
+    else:
+        lib.cb_paged_attention(*meta, k_cache, v_cache, out, scale, ws, max_q, max_kv)
     status = lib.cb_last_error()
     if check:
         assert status == 0, lib.cb_strerror(status)
