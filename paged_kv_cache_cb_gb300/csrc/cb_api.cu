@@ -97,13 +97,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Smallest decode split the launcher may choose; the workspace is sized for it.
 constexpr int kMinSplitBlocks = 8;
 
-WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int split_blocks) {
+namespace {
+
+// Offsets for a given capacity of split partials.
+WorkspaceLayout layout_for_splits(long long splits, int n_reqs, int n_q_heads, int n_kv_heads, int head_dim) {
   WorkspaceLayout L{};
-  const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
-  // a request's blocks are cut into pieces of >= split_blocks blocks at
-  // boundaries that need not start at its first block: one piece more at most
-  const long long splits = (long long)n_reqs * ((nblk + split_blocks - 1) / split_blocks + 1);
   L.max_splits_total = (int)splits;
   size_t off = 0;
   L.counters = off;
@@ -116,6 +114,36 @@ WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int 
   off = align_up(off + (size_t)splits * n_q_heads * head_dim * 4, 256);
   L.total = off;
   return L;
+}
+
+bool block_tile_shape(int n_q_heads, int n_kv_heads, int head_dim) {
+  return head_dim == 128 && n_kv_heads == 8 && n_q_heads / n_kv_heads >= 2;
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int split_blocks) {
+  const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
+  // a request's blocks are cut into pieces of >= split_blocks blocks at
+  // boundaries that need not start at its first block: one piece more at most
+  long long splits = (long long)n_reqs * ((nblk + split_blocks - 1) / split_blocks + 1);
+  // the block-tile decode cuts small steps into shorter chunks: at most
+  // 4 rounds of one chunk per CTA beyond that
+  if (block_tile_shape(n_q_heads, n_kv_heads, head_dim)) splits += 4LL * kMaxDecodeGrid + 8;
+  return layout_for_splits(splits, n_reqs, n_q_heads, n_kv_heads, head_dim);
+}
+
+// The same offsets with as many split partials as `bytes` can hold (at least
+// L's): a larger workspace than the size query asked for lets the decode cut
+// a step into more, shorter pieces.
+WorkspaceLayout workspace_layout_for_bytes(const WorkspaceLayout& L, size_t bytes, int n_reqs, int n_q_heads,
+                                           int n_kv_heads, int head_dim) {
+  const size_t per_split = (size_t)n_q_heads * (2 + head_dim) * 4;
+  if (bytes <= L.part_ml + 512) return L;
+  const long long fit = std::min<long long>((long long)((bytes - L.part_ml - 512) / per_split), 1LL << 24);
+  if (fit <= L.max_splits_total) return L;
+  return layout_for_splits(fit, n_reqs, n_q_heads, n_kv_heads, head_dim);
 }
 
 int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms) {
@@ -205,8 +233,9 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
     return CB_EINVAL;
   if (app && (!app->k_new || !app->v_new || !app->slots || !aligned16(app->k_new) || !aligned16(app->v_new)))
     return CB_EINVAL;
-  const WorkspaceLayout L = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8);
-  if (workspace_bytes < L.total) return CB_EWORKSPACE;
+  const WorkspaceLayout L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8);
+  if (workspace_bytes < L0.total) return CB_EWORKSPACE;
+  const WorkspaceLayout L = workspace_layout_for_bytes(L0, workspace_bytes, n_reqs, n_q_heads, n_kv_heads, head_dim);
   DeviceInfo di;
   if (!device_info(&di)) return CB_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -237,7 +266,7 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
   const int group = n_q_heads / n_kv_heads;
   // GQA with 8 KV heads and head_dim 128: decode tokens run the block-tile
   // pipeline (one block of all heads is one 128-row MMA tile)
-  const bool block_tiles = head_dim == 128 && n_kv_heads == 8 && group >= 2;
+  const bool block_tiles = block_tile_shape(n_q_heads, n_kv_heads, head_dim);
   // maps: [0, 1] K, V with 16-row boxes; [2] prefill q; [3, 4] K, V with
   // 128-row boxes; [5] decode q (one token, all heads)
   CUtensorMap maps[6];

@@ -384,6 +384,8 @@ __device__ __forceinline__ void append_pieces(const uint4* __restrict__ k_new, c
     const int64_t g = rem / chunks_per_row;
     const int64_t c = rem - g * chunks_per_row;
     const int64_t slot = __ldg(slots + t);
+    const uint4 kv = __ldg(k_new + i);           // in bounds whatever the slot: loaded with it
+    const uint4 vv = __ldg(v_new + i);
     if (slot < 0) continue;
     if (slot >= n_slots) {
       set_error(err, CB_DEVERR_BADSLOT);
@@ -391,8 +393,6 @@ __device__ __forceinline__ void append_pieces(const uint4* __restrict__ k_new, c
     }
     const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
     const int64_t dst = ((blk * n_kv_heads + g) * kBlockSize + off) * chunks_per_row + c;
-    const uint4 kv = __ldg(k_new + i);
-    const uint4 vv = __ldg(v_new + i);
     k_cache[dst] = kv;
     v_cache[dst] = vv;
   }

@@ -43,14 +43,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   append_wait(P, Ap);
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
-  run_pipeline<G>(P, &kmap, &vmap, &qmap, T, C, bpre, slot, tmem);
+  run_pipeline<G>(P, &kmap, &vmap, &qmap, T, C, bpre, slot, tmem, true);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg<G>::TM);
   }
-  merge_phase<G>(P, C, slot);
+  merge_phase<G>(P, C, slot, reinterpret_cast<float*>(&T.k[0][0][0][0]));   // the K ring is free now
 }
 
 template <int G>

@@ -50,8 +50,9 @@ namespace tcb {
 constexpr int kThreads = 352;
 constexpr int kMergeTid0 = 224;   // epilogue warps 7-10
 constexpr int kHkv = 8;
-constexpr int kChunksPerCta = 4;   // work chunks per CTA (before clamping W)
-constexpr int kMinChunk = 8;       // blocks; the partial buffers are sized for it
+constexpr int kChunksPerCta = 4;   // most rounds of chunks per CTA
+constexpr int kRoundBlocks = 8;    // blocks per CTA per round before a step takes another round
+constexpr int kMinChunk = 4;       // blocks
 
 template <int G>
 struct Cfg {
@@ -96,6 +97,7 @@ struct Ctl {
   } ep[2];                     // finished segments handed to the epilogue warps
   uint64_t ep_full[2], ep_empty[2], o_full[2], o_free[2];
   int merge_ok;                // every CTA reached the merge barrier in time
+  int split_any;               // some request is cut into several splits (merge phase needed)
   int W, NC, total;             // chunk size (blocks), number of chunks, blocks in all
   int mma_nbs[4];              // MMA issuer: lengths of the segments it is between
   uint32_t tmem_base;
@@ -176,19 +178,27 @@ __device__ inline int block_scan_excl(int* a, int n, int* scratch) {
 }
 
 // Given bpre[r] = decode blocks of request r (r < n), makes bpre the exclusive
-// prefix of blocks, picks the chunk size W (about kChunksPerCta
-// chunks per CTA, W in [kMinChunk, 32]) and makes slot the prefix of splits (a
-// request spanning chunks f..l has l - f + 1).  All threads call it; every CTA
-// computes the same plan.  Ends with __syncthreads().
+// prefix of blocks, picks the chunk size W and makes slot the prefix of splits
+// (a request spanning chunks f..l has l - f + 1).  W fills the grid in the
+// fewest rounds: R = ceil(total / (kRoundBlocks * grid)) rounds, at most
+// kChunksPerCta (more rounds balance larger steps dynamically), then
+// W = ceil(total / (R * grid)) in [kMinChunk, 32], raised if the partial
+// buffers could not hold the splits (n + chunks).  All threads call it; every
+// CTA computes the same plan.  Ends with __syncthreads().
 template <int G>
 __device__ void finish_plan(const StepParams& P, Ctl<G>& C, int* bpre, int* slot) {
   const int n = P.n_reqs, tid = threadIdx.x, T = blockDim.x;
   const int total = block_scan_excl(bpre, n, C.scratch);
-  const long long want = (total + (long long)kChunksPerCta * gridDim.x - 1) / ((long long)kChunksPerCta * gridDim.x);
+  const long long grid = gridDim.x;
+  const long long R = max(1LL, min((long long)kChunksPerCta, (total + kRoundBlocks * grid - 1) / (kRoundBlocks * grid)));
+  long long want = (total + R * grid - 1) / (R * grid);
+  const long long cap = max(1LL, (long long)P.max_splits_total - n);   // chunks the partial buffers can take
+  want = max(want, (total + cap - 1) / cap);
   const int W = (int)max((long long)kMinChunk, min((long long)kMaxSplitBlocks, want));
   for (int i = tid; i < n; i += T) {
     const int blk = bpre[i + 1] - bpre[i];
     slot[i] = blk > 0 ? (bpre[i] + blk - 1) / W - bpre[i] / W + 1 : 0;
+    if (slot[i] > 1) C.split_any = 1;
   }
   __syncthreads();
   const int splits = block_scan_excl(slot, n, C.scratch);
@@ -232,6 +242,7 @@ __device__ void init_ctl(Ctl<G>& C) {
   for (int s = 0; s < 3; ++s) mbar_init(&C.s_full[s], 1);
   mbar_init(&C.drain, 1);
   C.abort = 0;
+  C.split_any = 0;
 }
 template <int G>
 __device__ void zero_p(Tiles<G>& T) {
@@ -247,7 +258,7 @@ __device__ void zero_p(Tiles<G>& T) {
 // stalls the stream; claiming no earlier keeps the dynamic balance.
 template <int G>
 __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* qmap, Tiles<G>& T,
-                           Ctl<G>& C, const int* bpre, const int* slot) {
+                           Ctl<G>& C, const int* bpre, const int* slot, bool static_first) {
   constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS;
   constexpr uint32_t kTileBytes = 2 * 128 * 128;
   const unsigned FULL = 0xffffffffu;
@@ -275,13 +286,16 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
       cp_async4(&C.raw[buf].bt[lane], P.block_tables + (size_t)r * P.max_blocks_per_seq + b0 + lane);
     cp_async_commit();
   };
+  // With static_first, CTA b starts on chunk b and the counter hands out the
+  // chunks from gridDim.x on (no atomic round trip before the first load).
+  const int claim0 = static_first ? (int)gridDim.x : 0;
   auto claim = [&]() {
     int v = 0;
-    if (lane == 0) v = atomicAdd(P.queue, 1);
+    if (lane == 0) v = claim0 + atomicAdd(P.queue, 1);
     return v;                      // valid in lane 0
   };
   // segment cursor: chunk c (-1: none left), next linear block x, chunk end, request i
-  int c = __shfl_sync(FULL, claim(), 0), x = 0, end = 0, i = 0;
+  int c = static_first ? (int)blockIdx.x : __shfl_sync(FULL, claim(), 0), x = 0, end = 0, i = 0;
   if (c >= NC) c = -1;
   if (c >= 0) {
     x = c * W;
@@ -784,8 +798,10 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
 // (the TMA loads of the producers) on both sides of the counter.  Not inlined:
 // the copy loop's registers stay out of the pipeline's allocation.
 static __device__ __noinline__ void append_store(const AppendParams& Ap, int64_t n_slots, unsigned int* err) {
-  append_pieces(Ap.k_new, Ap.v_new, Ap.slots, Ap.n_tokens, Ap.k_cache, Ap.v_cache, n_slots, kHkv, 16, err,
-                blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+  const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i0 >= (int64_t)Ap.n_tokens * kHkv * 16) return;    // no piece for this thread: nothing to fence
+  append_pieces(Ap.k_new, Ap.v_new, Ap.slots, Ap.n_tokens, Ap.k_cache, Ap.v_cache, n_slots, kHkv, 16, err, i0,
+                (int64_t)gridDim.x * blockDim.x);
   fence_proxy_async_global();
   __threadfence();
 }
@@ -807,96 +823,151 @@ __device__ __forceinline__ void append_wait(const StepParams& P, const AppendPar
         set_error(P.err, CB_DEVERR_TIMEOUT);
         break;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
   }
   __syncthreads();
   fence_proxy_async_global();
 }
 
-// After the pipeline: a grid-wide barrier (the launch is cooperative, so every
-// CTA is resident; the wait is bounded), then every warp of the grid merges one
+// After the pipeline, when some request was cut into several splits (every CTA
+// made the same plan, so all take the same branch): a grid-wide barrier (the
+// launch is cooperative, so every CTA is resident; the wait is bounded; the
+// last CTA to arrive does not wait), then every warp of the grid merges one
 // (request, q head) of the requests cut into several splits at a time, by
 // log-sum-exp over the splits' partials (m: running max, l: sum, acc: O):
 //   out = sum_s 2^(m_s - M) acc_s / L,  M = max_s m_s,  L = sum_s 2^(m_s - M) l_s.
 // Lane = 4 output dimensions; eight splits' loads in flight.  All threads of
-// the CTA call it.
+// the CTA call it; red: nw * 128 floats of shared memory that nothing else
+// uses any more (the tile rings).
 template <int G>
-__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* slot) {
+__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* slot, float* red) {
   constexpr int Hq = Cfg<G>::Hq;
   const unsigned FULL = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!C.split_any) return;        // every output was written by its only split
   __syncthreads();
   if (threadIdx.x == 0) {
     C.merge_ok = 1;
     __threadfence();               // this CTA's partials before its arrival
-    atomicAdd(P.queue + 1, 1);
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(P.queue + 1) < gridDim.x) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        set_error(P.err, CB_DEVERR_TIMEOUT);
-        C.merge_ok = 0;
-        break;
+    if (atomicAdd(P.queue + 1, 1) + 1 < gridDim.x) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(P.queue + 1) < gridDim.x) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_error(P.err, CB_DEVERR_TIMEOUT);
+          C.merge_ok = 0;
+          break;
+        }
+        __nanosleep(32);
       }
-      __nanosleep(200);
+    } else {
+      __threadfence();             // last to arrive: the others' partials are released before their arrivals
     }
   }
   __syncthreads();
   if (!C.merge_ok) return;
   const int nw = blockDim.x >> 5;
   const int n_task = P.n_reqs * Hq;
-  for (int task = blockIdx.x * nw + warp; task < n_task; task += gridDim.x * nw) {
+  // Few tasks: a CTA per (request, head), its warps sharing the splits and
+  // adding their sums in shared memory (red: nw * 128 floats); else a warp per task.
+  const bool cta_mode = n_task <= (int)gridDim.x;
+  const int g = cta_mode ? nw : 1, sub = cta_mode ? warp : 0;
+  const int task0 = cta_mode ? (int)blockIdx.x : (int)blockIdx.x * nw + warp;
+  const int tstride = cta_mode ? (int)gridDim.x : (int)gridDim.x * nw;
+  for (int task = task0; task < n_task; task += tstride) {
     const int i = task / Hq, h = task - i * Hq;
     const int slot0 = slot[i], ns = slot[i + 1] - slot0;
-    if (ns <= 1) continue;
-    const float* ml = P.part_ml + ((size_t)slot0 * Hq + h) * 2;
+    if (ns <= 1) continue;         // the same for every warp of the task
+    // (m, l) of splits lane + 32k, k < 4, stay in registers; splits past 128 are re-read
+    const float2* ml = reinterpret_cast<const float2*>(P.part_ml) + (size_t)slot0 * Hq + h;
+    float2 v[4];
     float M = kNegInf;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(ml + (size_t)s * Hq * 2));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int sp = lane + 32 * k;
+      v[k] = sp < ns ? __ldcg(ml + (size_t)sp * Hq) : make_float2(kNegInf, 0.f);
+      M = fmaxf(M, v[k].x);
+    }
+    for (int sp = lane + 128; sp < ns; sp += 32) M = fmaxf(M, __ldcg(ml + (size_t)sp * Hq).x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
     float L = 0.f;
-    for (int s = lane; s < ns; s += 32) L += ex2(__ldcg(ml + (size_t)s * Hq * 2) - M) * __ldcg(ml + (size_t)s * Hq * 2 + 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (lane + 32 * k < ns) L += ex2(v[k].x - M) * v[k].y;
+    for (int sp = lane + 128; sp < ns; sp += 32) {
+      const float2 t = __ldcg(ml + (size_t)sp * Hq);
+      L += ex2(t.x - M) * t.y;
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
     const float inv = 1.f / L;
+    float wk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wk[k] = lane + 32 * k < ns ? ex2(v[k].x - M) * inv : 0.f;
+    // this warp's splits sub, sub + g, ...: eight loads in flight
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* src = reinterpret_cast<const float4*>(P.part_acc + ((size_t)slot0 * Hq + h) * 128) + lane;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      const int cnt = min(32, ns - s0);
-      const float w_lane = lane < cnt ? ex2(__ldcg(ml + (size_t)(s0 + lane) * Hq * 2) - M) * inv : 0.f;
-      for (int u = 0; u < cnt; u += 8) {
-        float4 v[8];
+    for (int s0 = sub; s0 < ns; s0 += 8 * g) {
+      float4 x[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          v[k] = u + k < cnt ? __ldcg(src + (size_t)(s0 + u + k) * Hq * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 8; ++u) {
+        const int sp = s0 + u * g;
+        x[u] = sp < ns ? __ldcg(src + (size_t)sp * Hq * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float w = __shfl_sync(FULL, w_lane, (u + k) & 31);
-          acc.x += w * v[k].x;
-          acc.y += w * v[k].y;
-          acc.z += w * v[k].z;
-          acc.w += w * v[k].w;
+      for (int u = 0; u < 8; ++u) {
+        const int sp = s0 + u * g;   // the same in every lane
+        if (sp >= ns) break;
+        float w;
+        if (sp < 128) {
+          const int k = sp >> 5;
+          w = __shfl_sync(FULL, k == 0 ? wk[0] : k == 1 ? wk[1] : k == 2 ? wk[2] : wk[3], sp & 31);
+        } else {
+          w = ex2(__ldcg(ml + (size_t)sp * Hq).x - M) * inv;
         }
+        acc.x += w * x[u].x;
+        acc.y += w * x[u].y;
+        acc.z += w * x[u].z;
+        acc.w += w * x[u].w;
       }
     }
     const int t = __ldg(P.cu_q_lens + i);
-    uint2 o;
-    o.x = pack_bf16(acc.x, acc.y);
-    o.y = pack_bf16(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(P.out + ((size_t)t * Hq + h) * 128 + lane * 4) = o;
+    uint2* dst = reinterpret_cast<uint2*>(P.out + ((size_t)t * Hq + h) * 128 + lane * 4);
+    if (cta_mode) {
+      float4* r4 = reinterpret_cast<float4*>(red);
+      r4[warp * 32 + lane] = acc;
+      __syncthreads();
+      if (warp == 0) {
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < nw; ++w) {
+          const float4 y = r4[w * 32 + lane];
+          sum.x += y.x;
+          sum.y += y.y;
+          sum.z += y.z;
+          sum.w += y.w;
+        }
+        *dst = make_uint2(pack_bf16(sum.x, sum.y), pack_bf16(sum.z, sum.w));
+      }
+      __syncthreads();             // red is reused by the next task
+    } else {
+      *dst = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+    }
   }
 }
 
 // The decode pipeline on all kThreads threads (warp roles above) over the plan
-// (bpre, slot of finish_plan).
+// (bpre, slot of finish_plan).  static_first: the CTAs enter together, so CTA b
+// takes chunk b without the counter (the mixed launch's CTAs enter after
+// prefill shares of different lengths and claim every chunk).
 // TMEM columns [tmem, tmem + 5 Hq) must be allocated to the CTA.
 template <int G>
 __device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
                              const CUtensorMap* qmap, Tiles<G>& T, Ctl<G>& C, const int* bpre, const int* slot,
-                             uint32_t tmem) {
+                             uint32_t tmem, bool static_first) {
   const int warp = threadIdx.x >> 5;
   if (warp == 4) {
-    b_producer<G>(P, kmap, qmap, T, C, bpre, slot);
+    b_producer<G>(P, kmap, qmap, T, C, bpre, slot, static_first);
   } else if (warp == 6) {
     v_producer<G>(P, vmap, T, C);
   } else if (warp >= 7) {

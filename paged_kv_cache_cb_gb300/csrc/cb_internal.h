@@ -69,6 +69,9 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                  int split_blocks);
+// L with as many split partials as `bytes` of workspace hold (never fewer).
+WorkspaceLayout workspace_layout_for_bytes(const WorkspaceLayout& L, size_t bytes, int n_reqs, int n_q_heads,
+                                           int n_kv_heads, int head_dim);
 int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms);
 
 // Kernel launchers (defined in the .cu files); return a cudaError_t.

@@ -612,14 +612,14 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
     tc_fence_after();
-    if (!C.abort) tcb::run_pipeline<G>(P, &kmap_b, &vmap_b, &qmap_d, T2, C2, a1, a2, tmem);
+    if (!C.abort) tcb::run_pipeline<G>(P, &kmap_b, &vmap_b, &qmap_d, T2, C2, a1, a2, tmem, false);
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
-    tcb::merge_phase<G>(P, C2, a2);
+    tcb::merge_phase<G>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
   } else {
     if (warp == 9) {
       tc_fence_after();
