@@ -522,10 +522,15 @@ def run_trace(args, world, rank, local):
               sl=torch.zeros(budget, dtype=torch.int64).pin_memory(),
               ev=torch.cuda.Event()) for _ in range(2)]
     scale = 1.0 / math.sqrt(a)
-    stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0, h2d=0, d2h=0)
+    stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0, h2d=0, d2h=0,
+                 kv_stored=0, kv_paged=0, kv_contig=0)
 
     def one_step(i, host_io=None):
         m = sched.step()
+        mem = sched.kv_memory(max_seq)          # held after this step: paged blocks vs a max-length reservation
+        stats["kv_stored"] += mem["stored"]
+        stats["kv_paged"] += mem["paged"]
+        stats["kv_contig"] += mem["contiguous"]
         b, t = len(m["req_ids"]), int(m["cu_q_lens"][-1]) if len(m["req_ids"]) else 0
         stats["preempted"] += m["n_preempted"]
         if t == 0:
@@ -649,6 +654,11 @@ def run_trace(args, world, rank, local):
                    "l2": "inputs larger than L2: each iteration reads every running request's K/V in 32 layers",
                    "parallelism": f"replicas x{world} (independent traces, no collective)"},
         "roofline": roof, "device_s": dev_s, "wall_s": wall,
+        "kv_memory": {"paged_waste": 1 - timed["kv_stored"] / max(1, timed["kv_paged"]),
+                      "contiguous_waste": 1 - timed["kv_stored"] / max(1, timed["kv_contig"]),
+                      "contiguous_max_seq_len": max_seq,
+                      "definition": "slots held but not stored, summed over steps: paged blocks taken only when "
+                                    "full vs a cache reserving max_seq_len slots per running request"},
         "cpu_baseline": None, "e2e": e2e, "gpu_launches": timed["launches"], "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

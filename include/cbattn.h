@@ -269,6 +269,18 @@ int cb_sched_free_blocks(const cb_sched* s);
 int cb_sched_request_info(const cb_sched* s, int req_id, int* produced, int* stored, int* preemptions,
                           int* state);
 
+/* KV-cache memory right now (after the last step), against a contiguous cache
+ * that reserves max_seq_len positions per request for its whole life ([KVB]
+ * 连续内存分配: TraditionalKVCache) where the paged pool takes a block only when
+ * the last one is full ([SM] PagedAttention 批处理).  out (host int64 [4]):
+ *  out[0] running requests,
+ *  out[1] tokens whose K/V the running requests have stored,
+ *  out[2] token slots in the blocks taken from the pool (held blocks x block_size),
+ *  out[3] token slots a contiguous cache would reserve (out[0] x max_seq_len).
+ * Paged waste = 1 - out[1] / out[2]; contiguous waste = 1 - out[1] / out[3].
+ * Returns CB_OK, or CB_EINVAL (null handle or out, max_seq_len < 1). */
+int cb_sched_kv_memory(const cb_sched* s, int max_seq_len, int64_t* out);
+
 #ifdef __cplusplus
 }
 #endif

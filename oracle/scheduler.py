@@ -133,6 +133,18 @@ class FCFSScheduler:
         self.waiting.append(req)
         self.waiting.sort(key=lambda r: r.rid)
 
+    # --- memory accounting ----------------------------------------------
+    def kv_memory(self, max_seq_len):
+        """KV memory after the last step, in token slots: running requests, tokens
+        they have stored, slots in the blocks taken from the pool, and the slots a
+        contiguous cache reserving max_seq_len positions per request would hold
+        ([KVB] 连续内存分配: the TraditionalKVCache reservation; [SM] PagedAttention
+        批处理: a block is taken only when the last one is full)."""
+        running = len(self.running)
+        stored = sum(r.stored for r in self.running)
+        paged = (self.num_blocks - len(self.free)) * self.bs
+        return dict(running=running, stored=stored, paged=paged, contiguous=running * int(max_seq_len))
+
     # --- one iteration ---------------------------------------------------
     def done(self):
         return not self.pending and not self.waiting and not self.running

@@ -46,6 +46,7 @@ SIGNATURES = [
     ("cb_sched_done", _c_int, [_vp]),
     ("cb_sched_free_blocks", _c_int, [_vp]),
     ("cb_sched_request_info", _c_int, [_vp, _c_int, _intp, _intp, _intp, _intp]),
+    ("cb_sched_kv_memory", _c_int, [_vp, _c_int, _i64p]),
 ]
 
 _LIB = None
@@ -337,6 +338,13 @@ class Scheduler:
         _check("cb_sched_request_info", lib().cb_sched_request_info(self._h, rid, *[ctypes.byref(v) for v in vals]))
         produced, stored, preemptions, state = (v.value for v in vals)
         return dict(produced=produced, stored=stored, preemptions=preemptions, state=self.STATES[state])
+
+    def kv_memory(self, max_seq_len):
+        """KV memory after the last step: dict(running, stored, paged, contiguous) in
+        token slots (cb_sched_kv_memory)."""
+        out = np.zeros(4, np.int64)
+        _check("cb_sched_kv_memory", lib().cb_sched_kv_memory(self._h, int(max_seq_len), out.ctypes.data_as(_i64p)))
+        return dict(running=int(out[0]), stored=int(out[1]), paged=int(out[2]), contiguous=int(out[3]))
 
     def step(self):
         nr, nt = ctypes.c_int(), ctypes.c_int()

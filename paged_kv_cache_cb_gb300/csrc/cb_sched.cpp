@@ -135,6 +135,18 @@ int cb_sched_request_info(const cb_sched* h, int req_id, int* produced, int* sto
   return CB_OK;
 }
 
+int cb_sched_kv_memory(const cb_sched* h, int max_seq_len, int64_t* out) {
+  if (!h || !out || max_seq_len < 1) return CB_EINVAL;
+  const Sched& s = h->s;
+  long long stored = 0;
+  for (int rid : s.running) stored += s.reqs[rid].stored;
+  out[0] = (int64_t)s.running.size();
+  out[1] = stored;
+  out[2] = (int64_t)(s.num_blocks - (int)s.free_list.size()) * s.bs;
+  out[3] = (int64_t)s.running.size() * max_seq_len;
+  return CB_OK;
+}
+
 int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
                   int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
                   int* n_tokens_out) {

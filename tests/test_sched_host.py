@@ -23,6 +23,7 @@ def _compare(tr, max_batch=None, max_steps=200000):
     o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free, max_batch=max_batch)
     maxblk = max(-(-(p + out - 1) // tr.block_size) for _, p, out in tr.requests)
     mb = max_batch or tr.token_budget
+    maxlen = max(p + out - 1 for _, p, out in tr.requests)
     s = L.Scheduler(tr.num_blocks, tr.block_size, tr.token_budget, mb, free, maxblk)
     for a, p, out in tr.requests:
         s.add_request(a, p, out)
@@ -44,6 +45,7 @@ def _compare(tr, max_batch=None, max_steps=200000):
         assert g["n_preempted"] == len(m.preempted)
         total_pre += g["n_preempted"]
         assert s.free_blocks() == len(o.free)
+        assert s.kv_memory(maxlen) == o.kv_memory(maxlen), n
         n += 1
         assert n < max_steps
     assert s.done()

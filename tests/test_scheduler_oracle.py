@@ -134,3 +134,34 @@ def test_block_ownership_is_exclusive_every_step():
         owned = [b for r in s.reqs for b in r.blocks]
         assert len(owned) == len(set(owned))
         assert sorted(owned + list(s.free)) == list(range(tr.num_blocks))
+
+
+def test_kv_memory_closed_form_single_request():
+    """[SM] §PagedAttention 批处理: blocks are taken only when the last one is full;
+    [KVB] §连续内存分配: a contiguous cache reserves max_seq_len slots per request.
+    A 20-token prompt with 5 outputs (24 positions in all) in blocks of 16."""
+    s = FCFSScheduler([(0, 20, 5)], token_budget=64, block_size=16, num_blocks=8, free_order=range(8))
+    s.step()                                     # the prompt: 20 stored, 2 blocks
+    assert s.kv_memory(24) == dict(running=1, stored=20, paged=32, contiguous=24)
+    for _ in range(3):
+        s.step()                                 # decodes at positions 20, 21, 22
+    assert s.kv_memory(24) == dict(running=1, stored=23, paged=32, contiguous=24)
+    s.step()                                     # position 23 is the last: finished, blocks returned
+    assert s.kv_memory(24) == dict(running=0, stored=0, paged=0, contiguous=0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_kv_memory_paged_waste_is_below_one_block_per_request(seed):
+    """Paged: each running request wastes only the tail of its last block
+    (< block_size slots); contiguous: max_seq_len minus what is stored."""
+    tr = wl.small_trace(seed)
+    s = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks,
+                      wl.free_order(tr.num_blocks, tr.seed))
+    maxlen = max(p + o - 1 for _, p, o in tr.requests)
+    while not s.done():
+        s.step()
+        m = s.kv_memory(maxlen)
+        per_req = sum(-(-r.stored // tr.block_size) * tr.block_size for r in s.running)
+        assert m["paged"] == per_req
+        assert 0 <= m["paged"] - m["stored"] <= m["running"] * (tr.block_size - 1)
+        assert m["stored"] <= m["contiguous"]
