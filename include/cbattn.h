@@ -78,6 +78,21 @@ int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mappi
                  void* k_cache, void* v_cache, int num_blocks, int n_kv_heads, int head_dim,
                  int block_size, void* stream);
 
+/* Copy whole KV blocks: for each pair i, block pairs[2i+1] of both caches
+ * becomes a copy of block pairs[2i] (every KV head, K and V) -- the
+ * copy-on-write of shared blocks that cb_sched_step_copies lists ([KVB] 思想:
+ * blocks shared through the block table).  Run it on the step's stream before
+ * the step's append, once per layer's caches.
+ *  pairs    device, int32 [n_pairs][2] (src, dst); the dsts are distinct and
+ *           none is a src of another pair (the pairs may be copied in any order)
+ *  n_pairs  0 .. 65535
+ *  k_cache, v_cache  device, bf16 cache layout above, 16-byte aligned
+ * Bit-exact.  A block id outside [0, num_blocks) skips its pair and sets the
+ * device error word (cb_last_error -> CB_EDEVICE).  Returns CB_OK, CB_EINVAL or
+ * CB_ECUDA. */
+int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks,
+                   int n_kv_heads, int head_dim, int block_size, void* stream);
+
 /* ---------------------------------------------------------------- attention
  * One attention step ([CB] Attention, Chunked prefill, Continuous batching):
  * for request r with ctx = ctx_lens[r] stored tokens and q_len new tokens, new
@@ -248,6 +263,27 @@ void cb_sched_destroy(cb_sched* s);
  * come in non-decreasing arrival_step order).  Returns the id or CB_EINVAL. */
 int cb_sched_add_request(cb_sched* s, int arrival_step, int prompt_len, int output_len);
 
+/* The same for a request whose first prefix_len prompt tokens are those of
+ * every request of prefix group `group` (a shared system prompt, [KVN]
+ * 与Prefix Caching的结合): their K/V are computed once and the blocks holding
+ * them are shared ([KVB] 思想: block tables point at the same blocks).
+ * group >= 0 with 1 <= prefix_len < prompt_len, one prefix_len per group;
+ * group -1 with prefix_len 0 is a request with no shared prefix.
+ * Scheduling with prefixes (applied within the rules above):
+ *  - after a step, the first request of a group whose stored tokens cover the
+ *    prefix publishes it (its blocks over positions [0, prefix_len) gain a
+ *    reference; blocks return to the free list when no request or published
+ *    prefix holds them);
+ *  - a request of the group admitted with nothing stored starts with the
+ *    published positions stored: whole blocks shared, a partial last block
+ *    copied first into a block of its own (copy-on-write), or, with no free
+ *    block for the copy, whole blocks only;
+ *  - a running request that needs a block when none is free first drops
+ *    published prefixes, oldest first, and only then preempts.
+ * Returns the id or CB_EINVAL. */
+int cb_sched_add_request_prefix(cb_sched* s, int arrival_step, int prompt_len, int output_len, int group,
+                                int prefix_len);
+
 /* Run one scheduling step and write its metadata into caller-owned host arrays:
  *  req_ids [max_batch], q_lens [max_batch], ctx_lens [max_batch],
  *  cu_q_lens [max_batch + 1], block_tables [max_batch][max_blocks_per_seq]
@@ -259,6 +295,13 @@ int cb_sched_add_request(cb_sched* s, int arrival_step, int prompt_len, int outp
 int cb_sched_step(cb_sched* s, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
                   int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
                   int* n_tokens_out);
+
+/* The block copies (copy-on-write of shared partial blocks) of the last
+ * cb_sched_step: pairs (src, dst) of block ids into host int32 [2 * max_pairs].
+ * They must run on the device (cb_copy_blocks, every layer's cache) before that
+ * step's append.  Returns the number of pairs, CB_ESTATE if more than
+ * max_pairs, or CB_EINVAL. */
+int cb_sched_step_copies(const cb_sched* s, int32_t* pairs, int max_pairs);
 
 /* 1 when no request is pending, waiting or running. */
 int cb_sched_done(const cb_sched* s);

@@ -54,6 +54,25 @@ pages leave these points open):
 6. Optional ``max_batch`` caps the number of requests in one step (each pass
    stops once the batch holds that many); by default only the token budget
    bounds the batch.
+7. Shared prompt prefixes ([KVN] §与Prefix Caching的结合: requests sharing a
+   system prompt compute its KV once; [KVB] §思想: sharing blocks is a matter of
+   pointing block tables at the same blocks).  A request may belong to a prefix
+   group whose first L prompt tokens it shares (1 <= L < prompt).  Blocks count
+   their holders (requests and published prefixes) and go back to the free list
+   when none is left:
+   - at the end of a step, the first request of a group whose stored tokens
+     reach L publishes the blocks covering positions [0, L) (one more holder
+     each);
+   - admitting a request of the group with nothing stored: it holds the
+     published whole blocks, and a partial last block is copied into a fresh
+     block of its own (copy-on-write, listed in the step's metadata for the
+     device to run before the append); with no free block for that copy only
+     whole blocks are shared.  It starts with the shared positions stored.  Its
+     first chunk is min(prompt + produced - shared, budget left, positions
+     that fit: the free blocks after the copy plus the room left in the copy);
+   - a running request needing a block when none is free first drops the
+     oldest published prefix (repeatedly) and only then preempts; admission
+     neither drops prefixes nor preempts.
 """
 from collections import deque
 from dataclasses import dataclass, field
@@ -72,6 +91,8 @@ class Request:
     blocks: list = field(default_factory=list)
     state: str = "pending"     # pending, waiting, running, finished, rejected
     preemptions: int = 0
+    group: int = -1            # prefix group (-1: none)
+    prefix_len: int = 0        # shared prompt positions of the group
 
     @property
     def remaining(self):
@@ -88,6 +109,7 @@ class StepMetadata:
     slot_mapping: np.ndarray  # int64 [sum(q_lens)]
     preempted: list           # request ids preempted during this step
     finished: list            # request ids that finished at the end of this step
+    copies: list = field(default_factory=list)   # (src, dst) block copies to run before the append
 
 
 def _blocks_for(n_tokens, block_size):
@@ -96,10 +118,15 @@ def _blocks_for(n_tokens, block_size):
 
 class FCFSScheduler:
     def __init__(self, requests, token_budget, block_size, num_blocks, free_order, max_batch=None):
-        """requests: iterable of (arrival_step, prompt_len, output_len), ids = index,
-        sorted by arrival.  free_order: the initial free-list order (a permutation
-        of range(num_blocks))."""
-        self.reqs = [Request(i, int(a), int(p), int(o)) for i, (a, p, o) in enumerate(requests)]
+        """requests: iterable of (arrival_step, prompt_len, output_len[, group,
+        prefix_len]), ids = index, sorted by arrival.  free_order: the initial
+        free-list order (a permutation of range(num_blocks))."""
+        self.reqs = []
+        for i, t in enumerate(requests):
+            a, p, o = (int(x) for x in t[:3])
+            g, pl = (int(t[3]), int(t[4])) if len(t) > 3 else (-1, 0)
+            assert g < 0 or 1 <= pl < p, "a shared prefix leaves at least one prompt token"
+            self.reqs.append(Request(i, a, p, o, group=g, prefix_len=pl if g >= 0 else 0))
         arrivals = [r.arrival for r in self.reqs]
         assert arrivals == sorted(arrivals), "requests must be given in arrival order"
         assert sorted(int(b) for b in free_order) == list(range(num_blocks))
@@ -108,21 +135,52 @@ class FCFSScheduler:
         self.bs = int(block_size)
         self.num_blocks = int(num_blocks)
         self.free = deque(int(b) for b in free_order)
+        self.holders = [0] * self.num_blocks
+        self.published = {}        # group -> (blocks, positions, publication number)
+        self.n_published = 0
         self.pending = deque(self.reqs)
         self.waiting = []          # kept in arrival (id) order, head first
         self.running = []          # kept in arrival (id) order
         self.now = 0
 
     # --- allocator -------------------------------------------------------
+    def _take(self):
+        b = self.free.popleft()
+        self.holders[b] = 1
+        return b
+
+    def _let_go(self, b):
+        self.holders[b] -= 1
+        if self.holders[b] == 0:
+            self.free.append(b)
+
     def _grow(self, req, n_tokens):
         need = _blocks_for(n_tokens, self.bs) - len(req.blocks)
         for _ in range(need):
-            req.blocks.append(self.free.popleft())
+            req.blocks.append(self._take())
 
     def _release(self, req):
         for b in req.blocks:
-            self.free.append(b)
+            self._let_go(b)
         req.blocks = []
+
+    def _drop_oldest_prefix(self):
+        if not self.published:
+            return False
+        g = min(self.published, key=lambda k: self.published[k][2])
+        blocks, _, _ = self.published.pop(g)
+        for b in blocks:
+            self._let_go(b)
+        return True
+
+    def _maybe_publish(self, req):
+        if req.group < 0 or req.group in self.published or req.stored < req.prefix_len:
+            return
+        blocks = req.blocks[:_blocks_for(req.prefix_len, self.bs)]
+        for b in blocks:
+            self.holders[b] += 1
+        self.published[req.group] = (list(blocks), req.prefix_len, self.n_published)
+        self.n_published += 1
 
     def _preempt(self, req):
         self._release(req)
@@ -159,6 +217,7 @@ class FCFSScheduler:
             self.waiting.append(r)
 
         budget = self.budget
+        copies = []                # copy-on-write (src, dst) of this step
         sched = []                 # (req, n_tokens, stored_before)
         scheduled_ids = set()
         preempted = []
@@ -178,6 +237,8 @@ class FCFSScheduler:
             if req.state != "running" or req.remaining != 1:
                 continue
             while _blocks_for(req.stored + 1, self.bs) - len(req.blocks) > len(self.free):
+                if self._drop_oldest_prefix():
+                    continue
                 v = victim(req.rid - 1)              # candidates include req itself
                 self._preempt(v)
                 preempted.append(v.rid)
@@ -198,6 +259,8 @@ class FCFSScheduler:
                 continue
             want = min(req.remaining, budget)
             while _blocks_for(req.stored + want, self.bs) - len(req.blocks) > len(self.free):
+                if self._drop_oldest_prefix():
+                    continue
                 v = victim(req.rid)
                 if v is None:
                     break
@@ -217,9 +280,25 @@ class FCFSScheduler:
             req = self.waiting[0]
             if req.rid in preempted:
                 break
-            n = min(req.remaining, budget, len(self.free) * self.bs)
+            pub = self.published.get(req.group) if req.stored == 0 and req.group >= 0 else None
+            shared = pub[1] if pub else 0
+            tail = shared % self.bs                 # positions in a partial last shared block
+            if tail and not self.free:
+                shared, tail = shared - tail, 0     # no block for the copy: whole blocks only
+            room = (len(self.free) - (1 if tail else 0)) * self.bs + (self.bs - tail if tail else 0)
+            n = min(req.prompt_len + req.produced - shared, budget, room)
             if n <= 0:
                 break
+            if shared:
+                whole = shared // self.bs
+                for b in pub[0][:whole]:
+                    self.holders[b] += 1
+                    req.blocks.append(b)
+                if tail:
+                    mine = self._take()
+                    copies.append((pub[0][whole], mine))
+                    req.blocks.append(mine)
+                req.stored = shared
             self.waiting.pop(0)
             req.state = "running"
             self.running.append(req)
@@ -243,11 +322,13 @@ class FCFSScheduler:
             slot_mapping=np.array(slots, dtype=np.int64),
             preempted=preempted,
             finished=[],
+            copies=copies,
         )
 
         # the forward pass happens here; then every scheduled request advances
         for req, n, _ in sched:
             req.stored += n
+            self._maybe_publish(req)
             if req.stored == req.prompt_len + req.produced:
                 req.produced += 1
             if req.produced == req.output_len:

@@ -25,6 +25,7 @@ _intp = ctypes.POINTER(ctypes.c_int)
 # (name, restype, argtypes) of every exported entry point, in header order
 SIGNATURES = [
     ("cb_kv_append", _c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp]),
+    ("cb_copy_blocks", _c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp]),
     ("cb_paged_attention", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                     _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     ("cb_paged_attention_workspace_size", _c_size, [_c_int] * 8),
@@ -42,7 +43,9 @@ SIGNATURES = [
     ("cb_sched_create", _vp, [_c_int, _c_int, _c_int, _c_int, _i32p]),
     ("cb_sched_destroy", None, [_vp]),
     ("cb_sched_add_request", _c_int, [_vp, _c_int, _c_int, _c_int]),
+    ("cb_sched_add_request_prefix", _c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int]),
     ("cb_sched_step", _c_int, [_vp, _i32p, _i32p, _i32p, _i32p, _i32p, _c_int, _i64p, _intp, _intp]),
+    ("cb_sched_step_copies", _c_int, [_vp, _i32p, _c_int]),
     ("cb_sched_done", _c_int, [_vp]),
     ("cb_sched_free_blocks", _c_int, [_vp]),
     ("cb_sched_request_info", _c_int, [_vp, _c_int, _intp, _intp, _intp, _intp]),
@@ -135,6 +138,20 @@ def cb_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
     if (hk2, a2) != (hk, a):
         raise ValueError("cache heads/head_dim differ from k_new")
     _check("cb_kv_append", lib().cb_kv_append(pk, pv, ps, n, ck, cv, nb, hk, a, bs, _stream(stream)))
+
+
+def cb_copy_blocks(pairs, k_cache, v_cache, stream=None):
+    """pairs: int32 CUDA tensor [n, 2] of (src, dst) block ids; caches bf16
+    [num_blocks, Hkv, block_size, A]: block dst becomes a copy of block src."""
+    torch = _t()
+    bf = torch.bfloat16
+    pp = _dev(pairs, torch.int32, "pairs", 2)
+    ck = _dev(k_cache, bf, "k_cache", 4)
+    cv = _dev(v_cache, bf, "v_cache", 4)
+    if pairs.shape[1] != 2 or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    nb, hk, bs, a = k_cache.shape
+    _check("cb_copy_blocks", lib().cb_copy_blocks(pp, pairs.shape[0], ck, cv, nb, hk, a, bs, _stream(stream)))
 
 
 def cb_paged_attention_workspace_size(n_reqs, n_tokens, max_q_len, max_kv_len, n_q_heads, n_kv_heads, head_dim,
@@ -309,6 +326,7 @@ class Scheduler:
         self._cu = np.zeros(max_batch + 1, np.int32)
         self._bt = np.zeros((max_batch, max_blocks_per_seq), np.int32)
         self._sm = np.zeros(token_budget, np.int64)
+        self._pairs = np.zeros((max_batch, 2), np.int32)
 
     def close(self):
         if self._h:
@@ -321,11 +339,20 @@ class Scheduler:
         except Exception:
             pass
 
-    def add_request(self, arrival_step, prompt_len, output_len):
-        rid = lib().cb_sched_add_request(self._h, int(arrival_step), int(prompt_len), int(output_len))
+    def add_request(self, arrival_step, prompt_len, output_len, group=-1, prefix_len=0):
+        """group >= 0: the first prefix_len prompt tokens are shared by the group."""
+        rid = lib().cb_sched_add_request_prefix(self._h, int(arrival_step), int(prompt_len), int(output_len),
+                                                int(group), int(prefix_len))
         if rid < 0:
-            raise CBError("cb_sched_add_request", rid)
+            raise CBError("cb_sched_add_request_prefix", rid)
         return rid
+
+    def step_copies(self):
+        """Copy-on-write pairs (src, dst) of the last step, int32 [n, 2]."""
+        n = lib().cb_sched_step_copies(self._h, self._pairs.ctypes.data_as(_i32p), self._pairs.shape[0])
+        if n < 0:
+            raise CBError("cb_sched_step_copies", n)
+        return self._pairs[:n].copy()
 
     def done(self):
         return bool(lib().cb_sched_done(self._h))

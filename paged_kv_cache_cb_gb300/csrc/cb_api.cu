@@ -192,6 +192,25 @@ int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mappi
   return CB_OK;
 }
 
+int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks, int n_kv_heads,
+                   int head_dim, int block_size, void* stream) {
+  if (n_pairs < 0 || n_pairs > 65535 || num_blocks <= 0 || n_kv_heads <= 0 || (head_dim != 64 && head_dim != 128) ||
+      block_size != kBlockSize)
+    return CB_EINVAL;
+  if (n_pairs == 0) {
+    g_last_launches = 0;
+    return CB_OK;
+  }
+  if (!pairs || !k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return CB_EINVAL;
+  DeviceInfo di;
+  if (!device_info(&di)) return CB_ECUDA;
+  if (launch_copy_blocks(pairs, n_pairs, k_cache, v_cache, num_blocks, n_kv_heads, head_dim, di.err,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CB_ECUDA;
+  g_last_launches = 1;
+  return CB_OK;
+}
+
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len, int n_q_heads,
                                          int n_kv_heads, int head_dim, int block_size) {
   if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||

@@ -6,6 +6,8 @@
 // 16-byte vector per thread, consecutive threads on consecutive 16-byte pieces of
 // the same row, so reads of k_new and writes into the 256-byte (A=128) cache rows
 // are both fully coalesced.  Bit-exact by construction.
+#include <algorithm>
+
 #include "cb_common.cuh"
 
 namespace cb {
@@ -31,6 +33,40 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t
   kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, n_tokens, static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), (int64_t)num_blocks * kBlockSize, n_kv_heads, chunks, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- block copies
+// Copy-on-write of shared blocks ([KVB] 思想: blocks shared through the block
+// table): cache block dst = block src, all KV heads, K and V.  grid.y = pair,
+// grid.x CTAs stride over the block's 16-byte pieces.  Bit-exact.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k_cache,
+                                                          uint4* __restrict__ v_cache, int num_blocks,
+                                                          int64_t pieces_per_block, unsigned int* __restrict__ err) {
+  const int src = __ldg(pairs + 2 * blockIdx.y), dst = __ldg(pairs + 2 * blockIdx.y + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(err, CB_DEVERR_BADBLOCK);
+    return;
+  }
+  const uint4* ks = k_cache + (int64_t)src * pieces_per_block;
+  const uint4* vs = v_cache + (int64_t)src * pieces_per_block;
+  uint4* kd = k_cache + (int64_t)dst * pieces_per_block;
+  uint4* vd = v_cache + (int64_t)dst * pieces_per_block;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < pieces_per_block;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 k = ks[i], v = vs[i];
+    kd[i] = k;
+    vd[i] = v;
+  }
+}
+
+cudaError_t launch_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks,
+                               int n_kv_heads, int head_dim, unsigned int* err, cudaStream_t stream) {
+  if (n_pairs == 0) return cudaSuccess;
+  const int64_t pieces = (int64_t)n_kv_heads * kBlockSize * head_dim / 8;
+  const int ctas = (int)std::min<int64_t>(8, (pieces + 255) / 256);
+  copy_blocks_kernel<<<dim3(ctas, n_pairs), 256, 0, stream>>>(pairs, static_cast<uint4*>(k_cache),
+                                                             static_cast<uint4*>(v_cache), num_blocks, pieces, err);
   return cudaGetLastError();
 }
 

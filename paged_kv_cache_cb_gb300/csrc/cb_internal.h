@@ -92,6 +92,8 @@ cudaError_t launch_decode_tcb(const StepParams& p, const AppendParams& ap, const
 // and the decode q map.
 cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, bool block_tiles,
                          int head_dim, int group, int n_sms, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks,
+                               int n_kv_heads, int head_dim, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
 cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream);
 

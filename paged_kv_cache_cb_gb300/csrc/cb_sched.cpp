@@ -22,8 +22,28 @@
 //     the first one that gets no token or was preempted in this step.
 // A preempted request frees all blocks, keeps its produced tokens and re-runs
 // prompt + produced tokens as a prefill later.  Free blocks are FIFO.
+//
+// Shared prompt prefixes ([KVN] 与Prefix Caching的结合: requests that share a
+// system prompt compute its K/V once; [KVB] 思想: blocks are shared by pointing
+// several block tables at them).  Blocks carry reference counts (requests and
+// published prefixes holding them) and return to the free list at zero.
+//  e. after a step, the first request of a prefix group whose stored tokens
+//     cover the group's prefix publishes it: the blocks holding positions
+//     [0, prefix) gain a reference;
+//  f. a request of the group admitted with nothing stored takes the published
+//     blocks: whole blocks by reference; a last, partial block is copied into a
+//     block of its own first (copy-on-write: the request will write its own
+//     tokens into that block), the copy listed for the caller to run before the
+//     step's append; with no free block for the copy it shares whole blocks
+//     only.  It starts with the shared positions stored;
+//  g. when a running request needs a block and none is free, published
+//     prefixes are dropped (oldest first) before a request is preempted.
+// The request that published a prefix keeps writing its own positions into
+// the shared partial block; those slots lie past the prefix, and every other
+// holder reads them from its own copy.
 #include <algorithm>
 #include <deque>
+#include <map>
 #include <vector>
 
 #include "../../include/cbattn.h"
@@ -34,14 +54,26 @@ enum State { kPending = 0, kWaiting = 1, kRunning = 2, kFinished = 3, kRejected 
 
 struct Req {
   int rid, arrival, prompt, output;
+  int group = -1, prefix = 0;          // shared prompt prefix: group and its length (0: none)
   int produced = 0, stored = 0, state = kPending, preemptions = 0;
   std::vector<int> blocks;
   int remaining() const { return prompt + produced - stored; }
 };
 
+// A published prefix: the blocks holding positions [0, tokens) of its group.
+struct Prefix {
+  std::vector<int> blocks;
+  int tokens = 0;
+  int order = 0;                       // publication order (the oldest is dropped first)
+};
+
 struct Sched {
   int num_blocks, bs, budget, max_batch;
   std::deque<int> free_list;
+  std::vector<int> ref;                // holders of each block
+  std::map<int, Prefix> prefixes;      // group -> published prefix
+  std::vector<int> copies;             // this step's copy-on-write pairs (src, dst)
+  int n_published = 0;
   std::vector<Req> reqs;
   size_t next_pending = 0;
   std::vector<int> waiting;   // request ids, ascending
@@ -50,16 +82,60 @@ struct Sched {
 
   int blocks_for(long long n) const { return (int)((n + bs - 1) / bs); }
 
+  int take() {
+    const int b = free_list.front();
+    free_list.pop_front();
+    ref[b] = 1;
+    return b;
+  }
+  void drop(int b) {
+    if (--ref[b] == 0) free_list.push_back(b);
+  }
   void grow(Req& r, long long n_tokens) {
     const int need = blocks_for(n_tokens) - (int)r.blocks.size();
-    for (int i = 0; i < need; ++i) {
-      r.blocks.push_back(free_list.front());
-      free_list.pop_front();
-    }
+    for (int i = 0; i < need; ++i) r.blocks.push_back(take());
   }
   void release(Req& r) {
-    for (int b : r.blocks) free_list.push_back(b);
+    for (int b : r.blocks) drop(b);
     r.blocks.clear();
+  }
+  // g. drop the oldest published prefix; false when there is none
+  bool evict_prefix() {
+    auto oldest = prefixes.end();
+    for (auto it = prefixes.begin(); it != prefixes.end(); ++it)
+      if (oldest == prefixes.end() || it->second.order < oldest->second.order) oldest = it;
+    if (oldest == prefixes.end()) return false;
+    for (int b : oldest->second.blocks) drop(b);
+    prefixes.erase(oldest);
+    return true;
+  }
+  // e. publish r's prefix if its group has none and r has stored it
+  void publish(const Req& r) {
+    if (r.group < 0 || r.prefix <= 0 || r.stored < r.prefix || prefixes.count(r.group)) return;
+    Prefix px;
+    px.tokens = r.prefix;
+    px.order = n_published++;
+    for (int i = 0; i < blocks_for(r.prefix); ++i) {
+      px.blocks.push_back(r.blocks[i]);
+      ref[r.blocks[i]]++;
+    }
+    prefixes[r.group] = px;
+  }
+  // f. attach `share` positions of prefix px to r (nothing stored yet); cow:
+  // the last shared block is partial and a free block is there for its copy
+  void attach(Req& r, const Prefix& px, int share, bool cow) {
+    const int whole = share / bs;
+    for (int i = 0; i < whole; ++i) {
+      r.blocks.push_back(px.blocks[i]);
+      ref[px.blocks[i]]++;
+    }
+    if (cow) {
+      const int b = take();
+      copies.push_back(px.blocks[whole]);
+      copies.push_back(b);
+      r.blocks.push_back(b);
+    }
+    r.stored = share;
   }
   static void insert_sorted(std::vector<int>& v, int rid) { v.insert(std::lower_bound(v.begin(), v.end(), rid), rid); }
   static void erase(std::vector<int>& v, int rid) {
@@ -98,23 +174,43 @@ cb_sched* cb_sched_create(int num_blocks, int block_size, int token_budget, int 
   h->s.bs = block_size;
   h->s.budget = token_budget;
   h->s.max_batch = max_batch;
+  h->s.ref.assign(num_blocks, 0);
   for (int i = 0; i < num_blocks; ++i) h->s.free_list.push_back(free_order[i]);
   return h;
 }
 
 void cb_sched_destroy(cb_sched* h) { delete h; }
 
-int cb_sched_add_request(cb_sched* h, int arrival_step, int prompt_len, int output_len) {
+int cb_sched_add_request_prefix(cb_sched* h, int arrival_step, int prompt_len, int output_len, int group,
+                                int prefix_len) {
   if (!h || arrival_step < 0 || prompt_len < 1 || output_len < 1) return CB_EINVAL;
+  if (group < -1 || (group >= 0 && (prefix_len < 1 || prefix_len >= prompt_len)) || (group < 0 && prefix_len != 0))
+    return CB_EINVAL;
   Sched& s = h->s;
   if (!s.reqs.empty() && arrival_step < s.reqs.back().arrival) return CB_EINVAL;
+  for (const Req& o : s.reqs)          // one prefix length per group
+    if (group >= 0 && o.group == group && o.prefix != prefix_len) return CB_EINVAL;
   Req r;
   r.rid = (int)s.reqs.size();
   r.arrival = arrival_step;
   r.prompt = prompt_len;
   r.output = output_len;
+  r.group = group;
+  r.prefix = group >= 0 ? prefix_len : 0;
   s.reqs.push_back(r);
   return r.rid;
+}
+
+int cb_sched_add_request(cb_sched* h, int arrival_step, int prompt_len, int output_len) {
+  return cb_sched_add_request_prefix(h, arrival_step, prompt_len, output_len, -1, 0);
+}
+
+int cb_sched_step_copies(const cb_sched* h, int32_t* pairs, int max_pairs) {
+  if (!h || max_pairs < 0 || (max_pairs > 0 && !pairs)) return CB_EINVAL;
+  const int n = (int)h->s.copies.size() / 2;
+  if (n > max_pairs) return CB_ESTATE;
+  for (int i = 0; i < 2 * n; ++i) pairs[i] = h->s.copies[i];
+  return n;
 }
 
 int cb_sched_done(const cb_sched* h) {
@@ -154,6 +250,7 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
       !n_tokens_out || max_blocks_per_seq < 1)
     return CB_EINVAL;
   Sched& s = h->s;
+  s.copies.clear();
   // a. arrivals
   while (s.next_pending < s.reqs.size() && s.reqs[s.next_pending].arrival <= s.now) {
     Req& r = s.reqs[s.next_pending++];
@@ -187,6 +284,7 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
       Req& r = s.reqs[rid];
       if (r.state != kRunning || r.remaining() != 1) continue;
       while (s.blocks_for((long long)r.stored + 1) - (int)r.blocks.size() > (int)s.free_list.size()) {
+        if (s.evict_prefix()) continue;
         const int v = victim(rid - 1);           // includes rid itself
         s.preempt(v);
         preempted.push_back(v);
@@ -208,6 +306,7 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
       if (r.state != kRunning || scheduled[rid] || r.remaining() <= 1) continue;
       const int want = std::min(r.remaining(), budget);
       while (s.blocks_for((long long)r.stored + want) - (int)r.blocks.size() > (int)s.free_list.size()) {
+        if (s.evict_prefix()) continue;
         const int v = victim(rid);
         if (v < 0) break;
         s.preempt(v);
@@ -227,9 +326,23 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
     const int rid = s.waiting.front();
     if (std::find(preempted.begin(), preempted.end(), rid) != preempted.end()) break;
     Req& r = s.reqs[rid];
-    const long long fit = (long long)s.free_list.size() * s.bs;
-    const int n = (int)std::min<long long>(std::min(r.remaining(), budget), fit);
+    // f. a published prefix of its group: whole blocks shared, a partial last one copied
+    const Prefix* px = nullptr;
+    if (r.stored == 0 && r.group >= 0) {
+      auto it = s.prefixes.find(r.group);
+      if (it != s.prefixes.end()) px = &it->second;
+    }
+    int share = px ? px->tokens : 0;
+    bool cow = share % s.bs != 0;
+    if (cow && s.free_list.empty()) {
+      share -= share % s.bs;
+      cow = false;
+    }
+    const long long fit =
+        (long long)((int)s.free_list.size() - (cow ? 1 : 0)) * s.bs + (cow ? s.bs - share % s.bs : 0);
+    const int n = (int)std::min<long long>(std::min(r.prompt + r.produced - share, budget), fit);
     if (n <= 0) break;
+    if (px && share > 0) s.attach(r, *px, share, cow);
     s.waiting.erase(s.waiting.begin());
     r.state = kRunning;
     Sched::insert_sorted(s.running, rid);
@@ -263,6 +376,7 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
   for (const Item& it : sched) {
     Req& r = s.reqs[it.rid];
     r.stored += it.n;
+    s.publish(r);                                // e.
     if (r.stored == r.prompt + r.produced) r.produced++;
     if (r.produced == r.output) {
       r.state = kFinished;

@@ -21,14 +21,15 @@ def _compare(tr, max_batch=None, max_steps=200000):
     L = _L()
     free = wl.free_order(tr.num_blocks, tr.seed)
     o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free, max_batch=max_batch)
-    maxblk = max(-(-(p + out - 1) // tr.block_size) for _, p, out in tr.requests)
+    maxblk = max(-(-(t[1] + t[2] - 1) // tr.block_size) for t in tr.requests)
     mb = max_batch or tr.token_budget
-    maxlen = max(p + out - 1 for _, p, out in tr.requests)
+    maxlen = max(t[1] + t[2] - 1 for t in tr.requests)
     s = L.Scheduler(tr.num_blocks, tr.block_size, tr.token_budget, mb, free, maxblk)
-    for a, p, out in tr.requests:
-        s.add_request(a, p, out)
+    for t in tr.requests:
+        s.add_request(*t)
     n = 0
     total_pre = 0
+    total_copies = 0
     while not o.done():
         assert not s.done()
         m = o.step()
@@ -46,6 +47,8 @@ def _compare(tr, max_batch=None, max_steps=200000):
         total_pre += g["n_preempted"]
         assert s.free_blocks() == len(o.free)
         assert s.kv_memory(maxlen) == o.kv_memory(maxlen), n
+        assert s.step_copies().tolist() == [list(c) for c in m.copies], n
+        total_copies += len(m.copies)
         n += 1
         assert n < max_steps
     assert s.done()
@@ -53,6 +56,7 @@ def _compare(tr, max_batch=None, max_steps=200000):
         info = s.request_info(r.rid)
         assert info["state"] == r.state and info["produced"] == r.produced
         assert info["preemptions"] == r.preemptions
+    _compare.copies = total_copies
     return n, total_pre
 
 
@@ -91,3 +95,42 @@ def test_cpp_scheduler_rejects_bad_free_list():
     L = _L()
     with pytest.raises(L.CBError):
         L.Scheduler(4, 16, 8, 8, [0, 1, 1, 3], 4)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_cpp_scheduler_shares_prefixes_like_the_oracle(seed):
+    """Prefix groups: shared blocks, copy-on-write pairs, dropped prefixes and
+    preemptions, identical to the oracle step by step."""
+    tr = wl.with_prefixes(wl.small_trace(seed, num_blocks=24 + 4 * (seed % 3)), 3, 20 + seed, seed=seed)
+    _compare(tr)
+    assert _compare.copies > 0 or (20 + seed) % 16 == 0
+
+
+def test_cpp_scheduler_prefix_trace_prefix():
+    """The first 300 steps of the 256-request trace with 8 shared 1000-token system prompts."""
+    _compare_steps(wl.with_prefixes(wl.trace(seed=0), 8, 1000, seed=0), 300)
+
+
+def _compare_steps(tr, steps):
+    L = _L()
+    free = wl.free_order(tr.num_blocks, tr.seed)
+    o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free)
+    maxblk = max(-(-(t[1] + t[2] - 1) // tr.block_size) for t in tr.requests)
+    s = L.Scheduler(tr.num_blocks, tr.block_size, tr.token_budget, tr.token_budget, free, maxblk)
+    for t in tr.requests:
+        s.add_request(*t)
+    for n in range(steps):
+        m, g = o.step(), s.step()
+        assert np.array_equal(g["req_ids"], m.req_ids) and np.array_equal(g["slot_mapping"], m.slot_mapping), n
+        assert np.array_equal(g["ctx_lens"], m.ctx_lens), n
+        assert s.step_copies().tolist() == [list(c) for c in m.copies], n
+
+
+def test_cpp_scheduler_rejects_bad_prefix():
+    L = _L()
+    s = L.Scheduler(8, 16, 32, 8, list(range(8)), 4)
+    with pytest.raises(L.CBError):
+        s.add_request(0, 10, 2, 0, 10)          # the prefix must leave a prompt token
+    s.add_request(0, 20, 2, 1, 5)
+    with pytest.raises(L.CBError):
+        s.add_request(0, 20, 2, 1, 6)           # one prefix length per group

@@ -165,3 +165,72 @@ def test_kv_memory_paged_waste_is_below_one_block_per_request(seed):
         assert m["paged"] == per_req
         assert 0 <= m["paged"] - m["stored"] <= m["running"] * (tr.block_size - 1)
         assert m["stored"] <= m["contiguous"]
+
+
+def test_prefix_sharing_worked_example():
+    """[KVN] §与Prefix Caching的结合 with [KVB] §思想 (blocks shared through the block
+    table): two requests share a 20-token system prompt in blocks of 16.  The
+    first stores it (blocks a, b; b holds positions 16..19 of it and then its own
+    tokens) and publishes it; the second holds block a, gets a copy of b in a
+    block of its own (copy-on-write: it will write its own tokens there) and
+    starts with 20 positions stored."""
+    reqs = [(0, 30, 3, 0, 20), (1, 25, 2, 0, 20)]
+    s = FCFSScheduler(reqs, token_budget=64, block_size=16, num_blocks=8, free_order=range(8))
+    m0 = s.step()
+    assert m0.q_lens.tolist() == [30] and m0.copies == []
+    a, b = s.reqs[0].blocks
+    assert s.published[0][:2] == ([a, b], 20)
+    m1 = s.step()                                    # request 0 decodes, request 1 is admitted
+    assert m1.req_ids.tolist() == [0, 1] and m1.q_lens.tolist() == [1, 5] and m1.ctx_lens.tolist() == [30, 20]
+    (src, dst), = m1.copies
+    assert src == b and dst not in (a, b)
+    assert m1.block_tables[1] == [a, dst]
+    assert s.holders[a] == 3 and s.holders[b] == 2 and s.holders[dst] == 1
+    # request 1's own positions 20..24 go to its copy, never into the shared blocks
+    assert m1.slot_mapping[1:].tolist() == [dst * 16 + p % 16 for p in range(20, 25)]
+
+
+def _held(s):
+    h = [0] * s.num_blocks
+    for r in s.running:
+        for b in r.blocks:
+            h[b] += 1
+    for blocks, _, _ in s.published.values():
+        for b in blocks:
+            h[b] += 1
+    return h
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefix_sharing_invariants(seed):
+    """Every block's holder count equals the running requests and published
+    prefixes that hold it; free blocks have none; no step writes a position a
+    published prefix shares; a request admitted onto a prefix starts with its
+    positions stored and the prefix's whole blocks first in its table."""
+    tr = wl.with_prefixes(wl.small_trace(seed, num_blocks=26), 3, 18 + 5 * seed, seed=seed)
+    s = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks,
+                      wl.free_order(tr.num_blocks, tr.seed))
+    shares = 0
+    while not s.done():
+        before = {g: (list(p[0]), p[1]) for g, p in s.published.items()}
+        m = s.step()
+        held = _held(s)
+        assert held == s.holders
+        assert all(s.holders[b] == 0 for b in s.free)
+        assert len(s.free) + sum(1 for h in held if h) == s.num_blocks
+        protected = set()                  # prefixes published through the whole step (none dropped)
+        for g, (blocks, n) in before.items():
+            if g in s.published and s.published[g][0] == blocks:
+                for p in range(n):
+                    protected.add(blocks[p // tr.block_size] * tr.block_size + p % tr.block_size)
+        assert not protected.intersection(m.slot_mapping.tolist())
+        for i, rid in enumerate(m.req_ids.tolist()):
+            r = s.reqs[rid]
+            if r.group in before and m.ctx_lens[i] > 0 and any(dst == m.block_tables[i][-1] or dst in m.block_tables[i]
+                                                               for _, dst in m.copies):
+                blocks, n = before[r.group]
+                whole = n // tr.block_size
+                assert m.block_tables[i][:whole] == blocks[:whole]
+                assert m.ctx_lens[i] == n
+                shares += 1
+    assert shares > 0 or all(p[1] % tr.block_size == 0 for p in before.values())

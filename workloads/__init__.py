@@ -244,3 +244,19 @@ def small_trace(seed, n_requests=24, num_blocks=20, token_budget=48, max_prompt=
     return TraceShape(f"small_trace{seed}", 1, 4, 4, 64, BLOCK_SIZE, token_budget, num_blocks,
                       tuple((int(a), int(p), int(o)) for a, p, o in zip(arrivals, prompts, outputs)),
                       seed)
+
+
+def with_prefixes(tr, n_groups, prefix_len, seed=0, share=1.0):
+    """The same trace with shared system prompts: each request (with probability
+    `share`) joins one of n_groups prefix groups, and its prompt becomes the
+    group's prefix_len tokens followed by its own prompt.  Requests become
+    (arrival, prompt, output, group, prefix_len), group -1 for none."""
+    rng = np.random.default_rng(seed + 7919)
+    out = []
+    for a, p, o in tr.requests:
+        if rng.random() < share:
+            out.append((a, p + prefix_len, o, int(rng.integers(n_groups)), prefix_len))
+        else:
+            out.append((a, p, o, -1, 0))
+    return TraceShape(tr.name + f"_prefix{n_groups}x{prefix_len}", tr.n_layers, tr.n_q_heads, tr.n_kv_heads,
+                      tr.head_dim, tr.block_size, tr.token_budget, tr.num_blocks, tuple(out), tr.seed)
