@@ -489,6 +489,8 @@ def run_trace(args, world, rank, local):
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream            # raw handle: the cheapest form for the per-layer calls
     tr = wl.trace(seed=args.seed + rank, pool_bytes=int(args.trace_pool_gb * wl.GB), n_layers=args.trace_layers)
+    if args.trace_prefix_groups > 0:       # shared system prompts: blocks shared, partial last block copied
+        tr = wl.with_prefixes(tr, args.trace_prefix_groups, args.trace_prefix_len, seed=args.seed + rank)
     nl, hq, hk, a, bs, budget = tr.n_layers, tr.n_q_heads, tr.n_kv_heads, tr.head_dim, tr.block_size, tr.token_budget
     nb = tr.num_blocks
     bf = torch.bfloat16
@@ -500,12 +502,12 @@ def run_trace(args, world, rank, local):
     kn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=bf) for _ in range(nl)]
     vn = [torch.randn((budget, hk, a), generator=g, device=dev, dtype=bf) for _ in range(nl)]
     out = torch.empty((budget, hq, a), dtype=bf, device=dev)
-    maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
-    max_seq = max(p + o - 1 for _, p, o in tr.requests)
+    maxblk = max(-(-(t[1] + t[2] - 1) // bs) for t in tr.requests)
+    max_seq = max(t[1] + t[2] - 1 for t in tr.requests)
     def new_scheduler():
         s = L.Scheduler(nb, bs, budget, min(budget, L.CB_MAX_REQS), wl.free_order(nb, tr.seed), maxblk)
-        for arr, p, o in tr.requests:
-            s.add_request(arr, p, o)
+        for t in tr.requests:
+            s.add_request(*(t[:3] if args.trace_no_share else t))
         return s
 
     sched = new_scheduler()
@@ -525,8 +527,13 @@ def run_trace(args, world, rank, local):
     stats = dict(tokens=0, dec=0, pre=0, steps=0, idle=0, launches=0, kv_bytes=0, flops=0, preempted=0, h2d=0, d2h=0,
                  kv_stored=0, kv_paged=0, kv_contig=0)
 
+    d_pairs = torch.zeros((budget, 2), dtype=torch.int32, device=dev)
+    for hb in h:
+        hb["pairs"] = torch.zeros((budget, 2), dtype=torch.int32).pin_memory()
+
     def one_step(i, host_io=None):
         m = sched.step()
+        pairs = sched.step_copies()             # copy-on-write of shared partial blocks, before the append
         mem = sched.kv_memory(max_seq)          # held after this step: paged blocks vs a max-length reservation
         stats["kv_stored"] += mem["stored"]
         stats["kv_paged"] += mem["paged"]
@@ -542,6 +549,10 @@ def run_trace(args, world, rank, local):
         hb["ctx"].numpy()[:b] = m["ctx_lens"]
         hb["bt"].numpy()[:b] = m["block_tables"]
         hb["sl"].numpy()[:t] = m["slot_mapping"]
+        npairs = len(pairs)
+        if npairs:
+            hb["pairs"].numpy()[:npairs] = pairs
+            d_pairs[:npairs].copy_(hb["pairs"][:npairs], non_blocking=True)
         d_cu[:b + 1].copy_(hb["cu"][:b + 1], non_blocking=True)
         d_ctx[:b].copy_(hb["ctx"][:b], non_blocking=True)
         d_bt[:b].copy_(hb["bt"][:b], non_blocking=True)
@@ -554,6 +565,9 @@ def run_trace(args, world, rank, local):
                 qn[layer][:t].copy_(host_io["q"][layer][:t], non_blocking=True)
                 kn[layer][:t].copy_(host_io["k"][layer][:t], non_blocking=True)
                 vn[layer][:t].copy_(host_io["v"][layer][:t], non_blocking=True)
+            if npairs:
+                L.cb_copy_blocks(d_pairs[:npairs], kc[layer], vc[layer], sh)
+                stats["launches"] += 1
             L.cb_kv_append_paged_attention(kn[layer][:t], vn[layer][:t], d_sl[:t], qn[layer][:t], d_cu[:b + 1],
                                            d_ctx[:b], d_bt[:b], kc[layer], vc[layer], out[:t], scale, ws, max_q,
                                            max_kv, sh)
@@ -585,6 +599,16 @@ def run_trace(args, world, rank, local):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
+    def finished_tokens():
+        """Requests finished so far and their prompt + output tokens."""
+        n = tok = 0
+        for rid, t in enumerate(tr.requests):
+            if sched.request_info(rid)["state"] == "finished":
+                n += 1
+                tok += t[1] + t[2]
+        return n, tok
+
+    fin0 = finished_tokens()
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -597,6 +621,7 @@ def run_trace(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    fin1 = finished_tokens()
     barrier(world)
     clocks = sampler.stop() if sampler else None
     status = L.cb_last_error(stream)
@@ -648,12 +673,19 @@ def run_trace(args, world, rank, local):
         "metric": METRIC, "value": timed["tokens"] * world / elapsed, "unit": UNIT, "n_gpus": world,
         "steps": timed["steps"], "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(1, timed["steps"]),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": TRACE_DESC, "n_layers": nl, "num_blocks": nb, "token_budget": budget,
+        "config": {"workload": TRACE_DESC + (
+                       f"; {args.trace_prefix_groups} groups sharing a {args.trace_prefix_len}-token system prompt"
+                       + (", computed in full (no sharing)" if args.trace_no_share else
+                          ", blocks shared, partial last block copied on write")
+                       if args.trace_prefix_groups > 0 else ""),
+                   "n_layers": nl, "num_blocks": nb, "token_budget": budget,
                    "decode_tokens": timed["dec"], "prefill_tokens": timed["pre"], "idle_steps": timed["idle"],
                    "preemptions": timed["preempted"],
                    "l2": "inputs larger than L2: each iteration reads every running request's K/V in 32 layers",
                    "parallelism": f"replicas x{world} (independent traces, no collective)"},
         "roofline": roof, "device_s": dev_s, "wall_s": wall,
+        "finished_in_timed_region": {"requests": fin1[0] - fin0[0], "prompt_plus_output_tokens": fin1[1] - fin0[1],
+                                     "requests_per_s": (fin1[0] - fin0[0]) / elapsed},
         "kv_memory": {"paged_waste": 1 - timed["kv_stored"] / max(1, timed["kv_paged"]),
                       "contiguous_waste": 1 - timed["kv_stored"] / max(1, timed["kv_contig"]),
                       "contiguous_max_seq_len": max_seq,
@@ -673,6 +705,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + ["trace"])
     ap.add_argument("--trace-pool-gb", type=float, default=60.0, help="trace: K+V pool of all layers")
     ap.add_argument("--trace-layers", type=int, default=32, help="trace: attention layers per iteration")
+    ap.add_argument("--trace-prefix-groups", type=int, default=0,
+                    help="trace: requests join this many groups sharing a system prompt (0: none)")
+    ap.add_argument("--trace-prefix-len", type=int, default=1000, help="trace: shared system prompt tokens")
+    ap.add_argument("--trace-no-share", action="store_true",
+                    help="trace with prefix groups: compute every prompt in full (no block sharing)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", action="store_true", help="skip the in-process HBM copy probe")
