@@ -137,7 +137,11 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
                        void* stream);
 
 /* Bytes of workspace cb_paged_attention needs for these sizes (0 on invalid
- * sizes).  Pure host function. */
+ * sizes).  Pure host function.  With max_q_len > 1 on the block-tile shapes (8
+ * KV heads, head_dim 128, G >= 2) it includes ~43 MB for the partial results of
+ * prefill tile pairs that the launch cuts at CTA boundaries to balance its CTAs;
+ * a workspace without that room (down to the size for max_q_len = 1 plus the
+ * rest) is accepted and the launch then keeps tile pairs whole. */
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
                                          int n_q_heads, int n_kv_heads, int head_dim, int block_size);
 
@@ -180,9 +184,10 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
  * workspace: the scratch (split-K partials and counters) comes from one
  * library-owned device array of CB_NOALLOC_SCRATCH_BYTES, held on every GPU that
  * loads the library until the process exits.  Nothing is allocated per call.
- *  - Sizes whose cb_paged_attention_workspace_size(...) exceeds
- *    CB_NOALLOC_SCRATCH_BYTES are rejected with CB_EWORKSPACE before anything
- *    is enqueued.
+ *  - Sizes whose smallest accepted workspace exceeds CB_NOALLOC_SCRATCH_BYTES
+ *    are rejected with CB_EWORKSPACE before anything is enqueued (without room
+ *    for the balanced prefill's partial results the launch keeps prefill tile
+ *    pairs whole).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
  *    first call before any stream capture.

@@ -99,15 +99,19 @@ constexpr int kMinSplitBlocks = 8;
 
 namespace {
 
-// Offsets for a given capacity of split partials.
-WorkspaceLayout layout_for_splits(long long splits, int n_reqs, int n_q_heads, int n_kv_heads, int head_dim) {
+// Offsets for a given capacity of split partials (and pre_slots prefill slots).
+WorkspaceLayout layout_for_splits(long long splits, int n_reqs, int n_q_heads, int n_kv_heads, int head_dim,
+                                  int pre_slots) {
   WorkspaceLayout L{};
   L.max_splits_total = (int)splits;
+  L.pre_slots = pre_slots;
   size_t off = 0;
   L.counters = off;
   off = align_up(off + (size_t)n_reqs * n_kv_heads * 4, 16);
   L.queue = off;
   off = align_up(off + 16, 256);
+  L.pre_part = off;
+  off = align_up(off + (size_t)pre_slots * kPreRows * (head_dim + 2) * 4, 256);
   L.part_ml = off;
   off = align_up(off + (size_t)splits * n_q_heads * 2 * 4, 256);
   L.part_acc = off;
@@ -123,7 +127,7 @@ bool block_tile_shape(int n_q_heads, int n_kv_heads, int head_dim) {
 }  // namespace
 
 WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int split_blocks) {
+                                 int split_blocks, bool prefill_split) {
   const long long nblk = (max_kv_len + kBlockSize - 1) / kBlockSize;
   // a request's blocks are cut into pieces of >= split_blocks blocks at
   // boundaries that need not start at its first block: one piece more at most
@@ -131,7 +135,8 @@ WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int 
   // the block-tile decode cuts small steps into shorter chunks: at most
   // 4 rounds of one chunk per CTA beyond that
   if (block_tile_shape(n_q_heads, n_kv_heads, head_dim)) splits += 4LL * kMaxDecodeGrid + 8;
-  return layout_for_splits(splits, n_reqs, n_q_heads, n_kv_heads, head_dim);
+  const int pre_slots = prefill_split && block_tile_shape(n_q_heads, n_kv_heads, head_dim) ? 2 * kMaxDecodeGrid : 0;
+  return layout_for_splits(splits, n_reqs, n_q_heads, n_kv_heads, head_dim, pre_slots);
 }
 
 // The same offsets with as many split partials as `bytes` can hold (at least
@@ -143,7 +148,7 @@ WorkspaceLayout workspace_layout_for_bytes(const WorkspaceLayout& L, size_t byte
   if (bytes <= L.part_ml + 512) return L;
   const long long fit = std::min<long long>((long long)((bytes - L.part_ml - 512) / per_split), 1LL << 24);
   if (fit <= L.max_splits_total) return L;
-  return layout_for_splits(fit, n_reqs, n_q_heads, n_kv_heads, head_dim);
+  return layout_for_splits(fit, n_reqs, n_q_heads, n_kv_heads, head_dim, L.pre_slots);
 }
 
 int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms) {
@@ -211,12 +216,27 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
   return CB_OK;
 }
 
+}  // extern "C"
+
+namespace cb {
+// Smallest workspace a step accepts (without the balanced prefill's partials).
+size_t workspace_min_bytes(int n_reqs, int n_tokens, int max_q_len, int max_kv_len, int n_q_heads, int n_kv_heads,
+                           int head_dim, int block_size) {
+  if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
+      !shape_ok(n_q_heads, n_kv_heads, head_dim, block_size))
+    return 0;
+  return workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks, false).total;
+}
+}  // namespace cb
+
+extern "C" {
+
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len, int n_q_heads,
                                          int n_kv_heads, int head_dim, int block_size) {
   if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
       !shape_ok(n_q_heads, n_kv_heads, head_dim, block_size))
     return 0;
-  return workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks).total;
+  return workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks, max_q_len > 1).total;
 }
 
 }  // extern "C"
@@ -252,7 +272,9 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
     return CB_EINVAL;
   if (app && (!app->k_new || !app->v_new || !app->slots || !aligned16(app->k_new) || !aligned16(app->v_new)))
     return CB_EINVAL;
-  const WorkspaceLayout L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8);
+  // the balanced prefill's partial results when the workspace has room for them
+  WorkspaceLayout L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8, max_q_len > 1);
+  if (workspace_bytes < L0.total) L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8, false);
   if (workspace_bytes < L0.total) return CB_EWORKSPACE;
   const WorkspaceLayout L = workspace_layout_for_bytes(L0, workspace_bytes, n_reqs, n_q_heads, n_kv_heads, head_dim);
   DeviceInfo di;
@@ -319,7 +341,7 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
     launches = 2;
   }
   // split arrival counters and the work queue start at zero every call
-  if (cudaMemsetAsync(ws + L.counters, 0, L.part_ml - L.counters, s) != cudaSuccess) return CB_ECUDA;
+  if (cudaMemsetAsync(ws + L.counters, 0, L.pre_part - L.counters, s) != cudaSuccess) return CB_ECUDA;
   cudaError_t e;
   if (max_q_len == 1 && block_tiles) {
     e = launch_decode_tcb(p, ap, maps[3], maps[4], maps[5], group, std::min(di.n_sms, kMaxDecodeGrid), s);
@@ -327,7 +349,12 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
     e = launch_decode(p, maps[0], maps[1], head_dim, group, di.n_sms, s);
   } else {
     if (!block_tiles) maps[3] = maps[4] = maps[5] = maps[0];   // unused by the kernel
-    e = launch_mixed(p, ap, maps, block_tiles, head_dim, group, block_tiles ? std::min(di.n_sms, kMaxDecodeGrid) : di.n_sms,
+    PrefillSplit ps{};
+    if (L.pre_slots > 0) {
+      ps.part = reinterpret_cast<float*>(ws + L.pre_part);
+      ps.slots = L.pre_slots;
+    }
+    e = launch_mixed(p, ap, ps, maps, block_tiles, head_dim, group, block_tiles ? std::min(di.n_sms, kMaxDecodeGrid) : di.n_sms,
                      s);
   }
   if (e != cudaSuccess) return CB_ECUDA;

@@ -62,13 +62,27 @@ struct AppendParams {
   int n_tokens;
 };
 
+// Partial results of prefill tile pairs cut at CTA boundaries (the mixed
+// launch's balanced prefill; part == nullptr: whole pairs round robin).  Slot
+// 2b holds CTA b's first piece, 2b + 1 its last: [2 * 128 rows][A] unnormalised
+// O, then [2 * 128 rows][2] (running max in base 2 with the scale, row sum).
+struct PrefillSplit {
+  float* part;
+  int slots;                    // capacity (slots)
+};
+constexpr int kPreRows = 2 * kTileM;   // rows of a tile pair
+
 // Workspace carving (byte offsets), shared by the size query and the launcher.
 struct WorkspaceLayout {
-  size_t counters, queue, part_ml, part_acc, total;
+  size_t counters, queue, pre_part, part_ml, part_acc, total;
   int max_splits_total;
+  int pre_slots;                // prefill partial slots (0: none)
 };
+// prefill_split: room for the balanced prefill's partial results.
 WorkspaceLayout workspace_layout(int n_reqs, int max_kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int split_blocks);
+                                 int split_blocks, bool prefill_split = false);
+size_t workspace_min_bytes(int n_reqs, int n_tokens, int max_q_len, int max_kv_len, int n_q_heads, int n_kv_heads,
+                           int head_dim, int block_size);
 // L with as many split partials as `bytes` of workspace hold (never fewer).
 WorkspaceLayout workspace_layout_for_bytes(const WorkspaceLayout& L, size_t bytes, int n_reqs, int n_q_heads,
                                            int n_kv_heads, int head_dim);
@@ -90,8 +104,8 @@ cudaError_t launch_decode_tcb(const StepParams& p, const AppendParams& ap, const
 // Mixed prefill + decode step.  maps: K, V with 16-row boxes, the prefill q
 // map, then (block_tiles: the block-tile decode phase) K, V with 128-row boxes
 // and the decode q map.
-cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, bool block_tiles,
-                         int head_dim, int group, int n_sms, cudaStream_t stream);
+cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const PrefillSplit& ps, const CUtensorMap* maps,
+                         bool block_tiles, int head_dim, int group, int n_sms, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks,
                                int n_kv_heads, int head_dim, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);

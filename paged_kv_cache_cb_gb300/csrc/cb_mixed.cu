@@ -72,6 +72,14 @@ struct MixedCtl {
   uint32_t tmem_base;
   volatile int abort;
   int scratch[96];
+  // this CTA's prefill work (PieceIter): balanced: units [pc_u0, pc_u0 + pc_len)
+  // starting at tile pc_j0 of item pc_item; else whole items from pc_item on
+  int pc_balanced, pc_item, pc_j0, pc_len, pc_L;
+  long long pc_u0;
+  // the item whose first piece this CTA ran and which goes on in later CTAs
+  int own_item, own_slot;
+  long long own_u;
+  long long scan[12];
 };
 
 struct PreItem {
@@ -95,6 +103,131 @@ __device__ __forceinline__ PreItem pre_item(const StepParams& P, const int* pre,
   I.kv_hi = I.ctx + I.tok_hi;
   I.nkt = (I.kv_hi + kTileN - 1) / kTileN;
   return I;
+}
+
+// Key tiles of tile pair pr of a request with ctx stored and q_len new tokens.
+__device__ __forceinline__ int pair_tiles(int ctx, int q_len, int pr, int tok_per_pair) {
+  const int tok_hi = min(q_len, (pr + 1) * tok_per_pair);
+  return (ctx + tok_hi + kTileN - 1) / kTileN;
+}
+// Key tiles of all of request r's prefill items (every KV head).
+__device__ __forceinline__ long long request_tiles(const StepParams& P, int r, int tok_per_pair) {
+  const int q0 = __ldg(P.cu_q_lens + r), q_len = __ldg(P.cu_q_lens + r + 1) - q0, ctx = __ldg(P.ctx_lens + r);
+  if (q_len <= 1 || ctx < 0) return 0;
+  long long t = 0;
+  for (int pr = 0, n = (q_len + tok_per_pair - 1) / tok_per_pair; pr < n; ++pr) t += pair_tiles(ctx, q_len, pr, tok_per_pair);
+  return t * P.n_kv_heads;
+}
+
+// A CTA's prefill pieces (item, key tiles [j0, j1)) in order.  Round robin:
+// whole items blockIdx.x, blockIdx.x + gridDim.x, ...  Balanced (the
+// cooperative launch with room for partial results): the concatenation of all
+// items' key tiles, in item order, cut into gridDim.x equal ranges of pc_L
+// units; the CTA's range may start and end inside items.
+struct PieceIter {
+  int item, j0, left, balanced, k;
+  long long u;                     // balanced: unit at which the next piece starts
+  __device__ explicit PieceIter(const MixedCtl& C)
+      : item(C.pc_item), j0(C.pc_j0), left(C.pc_len), balanced(C.pc_balanced), k(-1), u(C.pc_u0) {}
+  // next piece into I, [a, b); piece number k (0 first); ustart: its first unit
+  __device__ bool next(const StepParams& P, const int* pre, int n_pre, int tok_per_pair, PreItem& I, int& a, int& b,
+                       long long& ustart) {
+    if (item >= n_pre || (balanced && left <= 0)) return false;
+    I = pre_item(P, pre, item, tok_per_pair);
+    ++k;
+    if (balanced) {
+      a = j0;
+      b = min(I.nkt, j0 + left);
+      ustart = u;
+      u += b - a;
+      left -= b - a;
+      ++item;
+      j0 = 0;
+    } else {
+      a = 0;
+      b = I.nkt;
+      ustart = 0;
+      item += gridDim.x;
+    }
+    return true;
+  }
+};
+
+// Plan of the balanced prefill (all threads; ends with __syncthreads()).  U =
+// all items' key tiles; CTA b runs units [b L, b L + L), L = ceil(U / grid).
+// Balanced only with room for the partials, more items than CTAs and L >= 4;
+// otherwise round robin.  Every CTA takes the same decision.
+template <int TOK2>
+__device__ void prefill_plan(const StepParams& P, const PrefillSplit& S, MixedCtl& C, const int* pre) {
+  const int n = P.n_reqs, T = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n_pre = pre[n];
+  if (tid == 0) {
+    C.pc_balanced = 0;
+    C.pc_item = blockIdx.x;
+    C.pc_j0 = 0;
+    C.pc_len = 0;
+    C.pc_L = 0;
+    C.pc_u0 = 0;
+    C.own_item = -1;
+  }
+  if (S.part == nullptr || S.slots < 2 * (int)gridDim.x || n_pre <= (int)gridDim.x) {
+    __syncthreads();
+    return;
+  }
+  // exclusive scan of the tiles over contiguous request segments
+  const int seg = (n + T - 1) / T, lo = min(n, tid * seg), hi = min(n, lo + seg);
+  long long local = 0;
+  for (int r = lo; r < hi; ++r) local += request_tiles(P, r, TOK2);
+  long long incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) C.scan[wid] = incl;
+  __syncthreads();
+  long long before = 0, U = 0;
+  for (int w = 0; w < (T + 31) / 32; ++w) {
+    if (w < wid) before += C.scan[w];
+    U += C.scan[w];
+  }
+  const long long excl = before + incl - local;
+  const long long L = (U + gridDim.x - 1) / gridDim.x;
+  if (L >= 4 && U < (1LL << 40)) {                  // uniform: every thread of every CTA sees the same U
+    const long long u0 = (long long)blockIdx.x * L;
+    const long long len = max(0LL, min(U, u0 + L) - u0);
+    if (tid == 0) {
+      C.pc_balanced = 1;
+      C.pc_L = (int)L;
+      C.pc_u0 = u0;
+      C.pc_len = (int)len;
+      C.pc_item = n_pre;                            // past the end unless a start is found below
+    }
+    __syncthreads();
+    if (len > 0 && u0 >= excl && u0 < excl + local) {
+      long long acc = excl;
+      for (int r = lo; r < hi; ++r) {
+        const long long t = request_tiles(P, r, TOK2);
+        if (u0 < acc + t) {                         // r's items: pairs from the last down, KV heads inside
+          const int q0 = __ldg(P.cu_q_lens + r), q_len = __ldg(P.cu_q_lens + r + 1) - q0;
+          const int ctx = __ldg(P.ctx_lens + r), n_pairs = (q_len + TOK2 - 1) / TOK2;
+          long long off = u0 - acc;
+          for (int rem = 0; rem < n_pairs * P.n_kv_heads; ++rem) {
+            const int nkt = pair_tiles(ctx, q_len, n_pairs - 1 - rem / P.n_kv_heads, TOK2);
+            if (off < nkt) {
+              C.pc_item = pre[r] + rem;
+              C.pc_j0 = (int)off;
+              break;
+            }
+            off -= nkt;
+          }
+          break;
+        }
+        acc += t;
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // Bounded wait whose outcome is the same for all 32 lanes of the warp.
@@ -127,9 +260,12 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
   const int my_b = (lane / H) & 7, my_hf = lane % H;
   const bool issuer = lane < 8 * H;
   uint32_t kt = 0, it = 0;
-  for (int item = blockIdx.x; item < n_pre; item += gridDim.x, ++it) {
+  PieceIter pieces(C);
+  PreItem I;
+  int j0, j1;
+  long long u_start;
+  for (; pieces.next(P, pre, n_pre, 2 * TOK, I, j0, j1, u_start); ++it) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, 2 * TOK);
     int ok = 1;
     if (lane == 0) {
       ok = lane_wait(P, C, &C.q_empty, (it & 1) ^ 1);
@@ -145,8 +281,8 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
     if (!__shfl_sync(FULL, ok, 0)) break;
     const int nblk_hi = (I.kv_hi + kBlockSize - 1) / kBlockSize;
     int y = rows_total;
-    for (int j = 0; j < I.nkt; ++j, ++kt) {
-      if ((j & 3) == 0) {          // table entries for this tile and the next three
+    for (int j = j0; j < j1; ++j, ++kt) {
+      if (((j - j0) & 3) == 0) {   // table entries for this tile and the next three
         const int blk = j * 8 + lane;
         y = rows_total;            // past the extent: TMA fills zeros
         if (blk < nblk_hi) {
@@ -157,7 +293,7 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
             set_error(P.err, CB_DEVERR_BADBLOCK);
         }
       }
-      const int yb = __shfl_sync(FULL, y, (j & 3) * 8 + my_b);
+      const int yb = __shfl_sync(FULL, y, ((j - j0) & 3) * 8 + my_b);
       const int st = kt & 1;
       const uint32_t ph = (kt >> 1) & 1;
       ok = 1;
@@ -269,15 +405,18 @@ __device__ void mma_issuer(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C,
   MmaIssuer<A> M(P, T, C, tmem);
   uint32_t kt = 0, it = 0;
   bool ok = true;
-  for (int item = blockIdx.x; item < n_pre && ok; item += gridDim.x, ++it) {
+  PieceIter pieces(C);
+  PreItem I;
+  int j0, j1;
+  long long u_start;
+  for (; ok && pieces.next(P, pre, n_pre, 2 * TOK, I, j0, j1, u_start); ++it) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, 2 * TOK);
     if (!lane_wait(P, C, &C.q_full, it & 1)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    const int n = I.nkt;
+    const int n = j1 - j0;          // this piece's key tiles
     int ns0 = 0, ns1 = 0, np0 = 0, np1 = 0;     // next S / next PV per side
     bool q_released = false;
     uint64_t t_last = globaltimer_ns();
@@ -332,8 +471,8 @@ __device__ void mma_issuer(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C,
 
 // ---------------------------------------------------------------- softmax (warps 0-7)
 template <int A, int G>
-__device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& C, const int* pre, uint32_t tmem,
-                             int side) {
+__device__ void softmax_side(const StepParams& P, const PrefillSplit& S, PrefillTiles<A>& T, MixedCtl& C,
+                             const int* pre, uint32_t tmem, int side) {
   constexpr int TOK = kTileM / G;
   constexpr int H = A / 64;
   const unsigned FULL = 0xffffffffu;
@@ -346,16 +485,19 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
   const int Hq = P.n_q_heads;
   const float sl2 = P.scale_log2;
   uint32_t sc = 0;                                           // S tiles consumed (= global key tiles)
-  for (int item = blockIdx.x; item < n_pre; item += gridDim.x) {
+  PieceIter pieces(C);
+  PreItem I;
+  int j0, j1;
+  long long u_start;
+  while (pieces.next(P, pre, n_pre, 2 * TOK, I, j0, j1, u_start)) {
     if (C.abort) break;
-    const PreItem I = pre_item(P, pre, item, 2 * TOK);
     const int tok_l = row / G, gq = row % G;
     const int ti = I.tok_lo + side * TOK + tok_l;
     const bool valid_row = ti < I.tok_hi;
     const int pos = I.ctx + min(ti, I.tok_hi - 1);            // last key this row may see
     float m = kNegInf, l = 0.f;                               // m: running max, times scale*log2 e
     bool ok = true;
-    for (int j = 0; j < I.nkt; ++j, ++sc) {
+    for (int j = j0; j < j1; ++j, ++sc) {
       if (!warp_wait(P, &C.s_full[side], sc & 1)) {
         ok = false;
         break;
@@ -392,7 +534,7 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
         alpha = ex2(m - mn);
         m = mn;
       }
-      if (j > 0 && __any_sync(FULL, need)) {
+      if (j > j0 && __any_sync(FULL, need)) {
         // rescale O: the previous O += P V of this side must be complete
         if (!warp_wait(P, &C.o_done[side], (sc - 1) & 1)) {
           ok = false;
@@ -479,6 +621,36 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
       break;
     }
     tc_fence_after();
+    if (j0 > 0 || j1 < I.nkt) {
+      // a piece of an item cut at a CTA boundary: its unnormalised O and (m, l)
+      // go to this CTA's slot (2b: first piece, 2b + 1: last); the CTA that ran
+      // the item's first tiles merges the pieces after the grid-wide barrier
+      const int slot = 2 * (int)blockIdx.x + (pieces.k == 0 ? 0 : 1);
+      if (slot < S.slots) {
+        float* base = S.part + (size_t)slot * kPreRows * (A + 2);
+        float* orow_p = base + (size_t)(side * kTileM + row) * A;
+#pragma unroll 1
+        for (int c = 0; c < A / 32; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + o_col + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(orow_p + c * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        }
+        *reinterpret_cast<float2*>(base + (size_t)kPreRows * A + (side * kTileM + row) * 2) = make_float2(m, l);
+        if (j0 == 0 && side == 0 && row == 0) {
+          C.own_item = pieces.item - 1;
+          C.own_slot = slot;
+          C.own_u = u_start;
+        }
+      } else {
+        set_error(P.err, CB_DEVERR_BADLEN);
+      }
+      tc_fence_before();
+      mbar_arrive(&C.o_free[side]);
+      continue;
+    }
     const float inv = 1.f / l;
     uint16_t* orow = P.out + ((size_t)(I.q0 + ti) * Hq + (size_t)I.g * G + gq) * A;
 #pragma unroll 1
@@ -503,6 +675,50 @@ __device__ void softmax_side(const StepParams& P, PrefillTiles<A>& T, MixedCtl& 
   }
 }
 
+// After the grid-wide barrier, the CTA that ran the first tiles of an item cut
+// at CTA boundaries merges the item's pieces by log-sum-exp over their
+// partials (as the decode's split merge): per row, M = max_k m_k,
+// L = sum_k 2^(m_k - M) l_k, out = sum_k 2^(m_k - M) O_k / L.  The item's
+// pieces are in CTAs b .. (item end - 1) / L: this CTA's own slot, then slot
+// 2c (the first piece) of each later CTA c.  All threads of the CTA call it.
+template <int A, int G>
+__device__ void prefill_merge(const StepParams& P, const PrefillSplit& S, const MixedCtl& C, const int* pre) {
+  constexpr int TOK = kTileM / G, Q = A / 4;
+  if (!C.pc_balanced || C.own_item < 0) return;
+  const PreItem I = pre_item(P, pre, C.own_item, 2 * TOK);
+  const int c0 = blockIdx.x, c1 = (int)((C.own_u + I.nkt - 1) / C.pc_L);
+  const size_t slot_floats = (size_t)kPreRows * (A + 2);
+  for (int task = threadIdx.x; task < kPreRows * Q; task += blockDim.x) {
+    const int row = task / Q, ch = task - row * Q;
+    const int side = row / kTileM, i = row - side * kTileM;
+    const int ti = I.tok_lo + side * TOK + i / G;
+    if (ti >= I.tok_hi) continue;
+    float M = kNegInf;
+    for (int c = c0; c <= c1; ++c) {
+      const int slot = c == c0 ? C.own_slot : 2 * c;
+      if (slot < S.slots) M = fmaxf(M, __ldcg(S.part + slot * slot_floats + (size_t)kPreRows * A + row * 2));
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c <= c1; ++c) {
+      const int slot = c == c0 ? C.own_slot : 2 * c;
+      if (slot >= S.slots) continue;
+      const float* base = S.part + slot * slot_floats;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + (size_t)kPreRows * A) + row);
+      const float w = ex2(ml.x - M);             // 0 for a piece in which the row saw no key
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(base + (size_t)row * A) + ch);
+      L += w * ml.y;
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+    const float inv = 1.f / L;
+    uint16_t* orow = P.out + ((size_t)(I.q0 + ti) * P.n_q_heads + (size_t)I.g * G + i % G) * A + ch * 4;
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  }
+}
+
 // Shared memory of the mixed kernel: the tile region (prefill tiles, or the
 // decode pipeline's rings in phase 2), the control blocks and the plan arrays.
 template <int A, int G, bool BT>
@@ -524,7 +740,7 @@ constexpr size_t mixed_smem(int n_reqs) {
 
 template <int A, int G, bool BT>
 __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
-    mixed_kernel(const StepParams P, const AppendParams Ap, const __grid_constant__ CUtensorMap kmap,
+    mixed_kernel(const StepParams P, const AppendParams Ap, const PrefillSplit Sp, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap,
                  const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_b,
                  const __grid_constant__ CUtensorMap vmap_b, const __grid_constant__ CUtensorMap qmap_d) {
@@ -558,6 +774,13 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     }
     mbar_init(&C.drain, 1);
     C.abort = 0;
+    C.pc_balanced = 0;             // prefill pieces: whole items round robin unless the plan balances them
+    C.pc_item = blockIdx.x;
+    C.pc_j0 = 0;
+    C.pc_len = 0;
+    C.pc_L = 0;
+    C.pc_u0 = 0;
+    C.own_item = -1;
     if constexpr (BT) {
       tcb::init_ctl<G>(*reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl)));
       prefetch_tmap(&kmap_b);
@@ -585,6 +808,8 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     __syncthreads();
     tcb::block_scan_excl(pre, P.n_reqs, C2.scratch);
     tcb::finish_plan<G>(P, C2, a1, a2);
+    prefill_plan<2 * TOK>(P, Sp, C, pre);
+    if (threadIdx.x == 0 && C.pc_balanced) C2.split_any = 1;   // the pieces' merge needs the grid-wide barrier
     tcb::append_wait(P, Ap);       // before the first TMA load of the cache
   } else {
     build_plan(P, 2 * TOK, a0, a1, a2, C.scratch);   // ends with __syncthreads()
@@ -599,7 +824,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
       if (lane == 0) mma_issuer<A, G>(P, T, C, pre, tmem);
       __syncwarp();
     } else if (warp < 8) {
-      softmax_side<A, G>(P, T, C, pre, tmem, warp >> 2);
+      softmax_side<A, G>(P, Sp, T, C, pre, tmem, warp >> 2);
     }
   }
   tc_fence_before();
@@ -620,6 +845,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
       tmem_dealloc(tmem, 512);
     }
     tcb::merge_phase<G>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
+    if (C.pc_balanced && C2.merge_ok) prefill_merge<A, G>(P, Sp, C, pre);
   } else {
     if (warp == 9) {
       tc_fence_after();
@@ -634,8 +860,8 @@ static_assert(mixed_smem<128, 4, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared 
 static_assert(mixed_smem<128, 8, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 
 template <int A, int G, bool BT>
-cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, int n_sms,
-                           cudaStream_t stream) {
+cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const PrefillSplit& ps, const CUtensorMap* maps,
+                           int n_sms, cudaStream_t stream) {
   const size_t smem = mixed_smem<A, G, BT>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
   if (!BT && ap.n_tokens != 0) return cudaErrorInvalidValue;   // only the cooperative launch stores rows
@@ -649,25 +875,26 @@ cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const CU
   if constexpr (BT) {   // cooperative: the decode merge phase waits for every CTA
     StepParams pc = p;
     AppendParams apc = ap;
-    void* args[] = {&pc, &apc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
+    PrefillSplit psc = ps;
+    void* args[] = {&pc, &apc, &psc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
                     const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
                     const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5])};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), dim3(n_sms),
                                        dim3(tcb::kThreads), args, smem, stream);
   } else {
-    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, ap, maps[0], maps[1], maps[2], maps[3],
-                                                                   maps[4], maps[5]);
+    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, ap, PrefillSplit{}, maps[0], maps[1], maps[2],
+                                                                   maps[3], maps[4], maps[5]);
     return cudaGetLastError();
   }
 }
 
 }  // namespace
 
-cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const CUtensorMap* maps, bool block_tiles,
-                         int head_dim, int group, int n_sms, cudaStream_t stream) {
+cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const PrefillSplit& ps, const CUtensorMap* maps,
+                         bool block_tiles, int head_dim, int group, int n_sms, cudaStream_t stream) {
 #define CB_MIX_CASE(A_, G_, BT_)                  \
   if (head_dim == A_ && group == G_ && block_tiles == BT_) \
-    return launch_mixed_t<A_, G_, BT_>(p, ap, maps, n_sms, stream);
+    return launch_mixed_t<A_, G_, BT_>(p, ap, ps, maps, n_sms, stream);
   CB_MIX_CASE(128, 2, true)
   CB_MIX_CASE(128, 4, true)
   CB_MIX_CASE(128, 8, true)

@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "../../include/cbattn.h"
+#include "cb_internal.h"
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CB_NOALLOC_SCRATCH_BYTES];
 
@@ -50,8 +51,9 @@ extern "C" int cb_paged_attention_noalloc(const void* q, const int32_t* cu_q_len
                                           int n_tokens, int max_q_len, int max_kv_len, const void* k_cache,
                                           const void* v_cache, int num_blocks, void* out, float scale, int n_q_heads,
                                           int n_kv_heads, int head_dim, int block_size, void* stream) {
-  const size_t need = cb_paged_attention_workspace_size(n_reqs, n_tokens, max_q_len, max_kv_len, n_q_heads,
-                                                        n_kv_heads, head_dim, block_size);
+  // the step falls back to whole prefill pairs when the partials do not fit
+  const size_t need = cb::workspace_min_bytes(n_reqs, n_tokens, max_q_len, max_kv_len, n_q_heads, n_kv_heads,
+                                              head_dim, block_size);
   if (need == 0) return CB_EINVAL;
   if (need > (size_t)CB_NOALLOC_SCRATCH_BYTES) return CB_EWORKSPACE;   // sizes beyond the fixed scratch
   void* ws = scratch_address();
