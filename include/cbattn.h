@@ -139,9 +139,9 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
 /* Bytes of workspace cb_paged_attention needs for these sizes (0 on invalid
  * sizes).  Pure host function.  With max_q_len > 1 on the block-tile shapes (8
  * KV heads, head_dim 128, G >= 2) it includes ~43 MB for the partial results of
- * prefill tile pairs that the launch cuts at CTA boundaries to balance its CTAs;
- * a workspace without that room (down to the size for max_q_len = 1 plus the
- * rest) is accepted and the launch then keeps tile pairs whole. */
+ * prefill tile pairs that the launch cuts at CTA boundaries to balance its CTAs.
+ * A workspace that is smaller by up to that region is still accepted; the launch
+ * then keeps every tile pair whole. */
 size_t cb_paged_attention_workspace_size(int n_reqs, int n_tokens, int max_q_len, int max_kv_len,
                                          int n_q_heads, int n_kv_heads, int head_dim, int block_size);
 

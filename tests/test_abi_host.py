@@ -67,6 +67,32 @@ def test_host_side_argument_checks():
     assert L.cb_paged_attention(*args(wsb=16)) == -3                # workspace too small
     assert L.cb_paged_attention(*args(nr=0)) == 0                   # empty batch: nothing to do
     assert L.cb_strerror(-3) == b"workspace too small"
+    # the one-call step: the append arguments are checked too
+    fargs = lambda **kw: [kw.get("kn", dummy), kw.get("vn", dummy), kw.get("sl", dummy)] + args(**kw)
+    assert L.cb_kv_append_paged_attention(*fargs(kn=None)) == -1
+    assert L.cb_kv_append_paged_attention(*fargs(vn=V(4104))) == -1   # not 16-byte aligned
+    assert L.cb_kv_append_paged_attention(*fargs(a=96)) == -1
+    assert L.cb_kv_append_paged_attention(*fargs(wsb=16)) == -3
+    assert L.cb_kv_append_paged_attention(*fargs(nr=0)) == 0
+    # block copies
+    assert L.cb_copy_blocks(dummy, -1, dummy, dummy, 8, 8, 128, 16, None) == -1
+    assert L.cb_copy_blocks(dummy, 1, dummy, dummy, 8, 8, 96, 16, None) == -1
+    assert L.cb_copy_blocks(dummy, 1, dummy, V(4100), 8, 8, 128, 16, None) == -1
+    assert L.cb_copy_blocks(None, 0, None, None, 8, 8, 128, 16, None) == 0   # nothing to copy
+
+
+def test_workspace_size_query_includes_the_prefill_partials():
+    """Block-tile shapes with prefill: the size query leaves room for the balanced
+    prefill's partial results (2 x 160 slots of 256 rows x (A + 2) floats); a
+    decode-only step or another shape needs none."""
+    L = _lib().lib()
+    region = 2 * 160 * 256 * (128 + 2) * 4
+    with_pre = L.cb_paged_attention_workspace_size(4, 600, 512, 4096, 32, 8, 128, 16)
+    dec = L.cb_paged_attention_workspace_size(4, 600, 1, 4096, 32, 8, 128, 16)
+    assert with_pre - dec >= region
+    mha_pre = L.cb_paged_attention_workspace_size(4, 600, 512, 4096, 32, 32, 128, 16)
+    mha_dec = L.cb_paged_attention_workspace_size(4, 600, 1, 4096, 32, 32, 128, 16)
+    assert mha_pre == mha_dec
 
 
 def test_workspace_size_grows_with_requests_and_context():
