@@ -393,8 +393,9 @@ def test_polynomial_exp2_against_cuda_exp2():
 # ------------------------------------------------------------------ balanced prefill pieces
 # With more tile pairs than CTAs, the cooperative launch cuts the pairs' key
 # tiles into equal ranges per CTA; pieces cut at CTA boundaries are merged by
-# log-sum-exp after the grid-wide barrier.  Sizes chosen for 160+ pairs with
-# short contexts, so that the oracle checks every row.
+# log-sum-exp after the grid-wide barrier.  Sizes chosen for 160-240 pairs
+# (pairs cut across up to 3 CTAs), small enough for the oracle to check every
+# row.
 _PRE_REGION = 2 * 160 * 256 * (128 + 2) * 4          # the partials' workspace region (A = 128)
 
 
@@ -403,7 +404,11 @@ _PRE_REGION = 2 * 160 * 256 * (128 + 2) * 4          # the partials' workspace r
     (32, (1280,), (100,)),                               # G = 4: 64-token pairs
     (64, (640,), (100,)),                                # G = 8: 32-token pairs
     (32, (1, 700, 1, 600, 1), (3000, 40, 20, 0, 900)),   # with decodes in the same launch
-], ids=["g2", "g4", "g8", "mixed"])
+    (16, (3840,), (0,)),                                 # 240 pairs
+    (32, (1600,), (1700,)),                              # 200 pairs over longer contexts
+    (64, (800,), (1700,)),
+    (32, (1, 1000, 1, 700, 1), (3000, 1500, 20, 800, 900)),
+], ids=["g2", "g4", "g8", "mixed", "g2_240", "g4_200", "g8_200", "mixed_216"])
 def test_balanced_prefill_pieces_match_oracle(hq, q_lens, ctx_lens):
     blocks = sum(-(-(c + q) // 16) for c, q in zip(ctx_lens, q_lens)) + 8
     shape = wl.StepShape(f"balanced_h{hq}", hq, 8, 128, 16, blocks, q_lens=q_lens, ctx_lens=ctx_lens, seed=hq)
@@ -412,7 +417,7 @@ def test_balanced_prefill_pieces_match_oracle(hq, q_lens, ctx_lens):
 
 def test_prefill_without_room_for_pieces_keeps_pairs_whole():
     """A workspace without the partials' region: the launch keeps tile pairs whole."""
-    shape = wl.StepShape("whole_pairs", 32, 8, 128, 16, 100, q_lens=(1280,), ctx_lens=(100,), seed=5)
+    shape = wl.StepShape("whole_pairs", 32, 8, 128, 16, 240, q_lens=(1600,), ctx_lens=(1700,), seed=5)
     inp = wl.step_inputs_cpu(shape)
     out, _, _, _ = device_step(shape, inp, ws_extra=-_PRE_REGION)
     assert_close(f64(out), oracle_step(shape, inp), shape.name)
