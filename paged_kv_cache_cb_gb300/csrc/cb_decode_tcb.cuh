@@ -15,9 +15,9 @@
 // and the softmax threads rewrite only the diagonal entries.
 //
 // Work: the decode requests' blocks, laid end to end in request order and cut
-// into equal chunks of W blocks (W in [8, 32], about four chunks per
-// CTA); one CTA (11 warps) per SM, persistent, takes chunks from a global
-// counter.  A chunk is one or more segments (request r, blocks [b0, b0+nb));
+// into equal chunks of W blocks (W in [4, 32], chosen to fill the grid in the
+// fewest rounds, at most four); one CTA (11 warps) per SM, persistent, takes
+// chunks from a global counter (the decode kernel's CTA b starts with chunk b).  A chunk is one or more segments (request r, blocks [b0, b0+nb));
 // a request cut into several segments leaves split partials, merged by the
 // whole grid once every chunk is done.  Equal chunks keep the CTAs' finishing
 // times together.  The chunk boundaries depend only on the step's lengths, so
@@ -37,8 +37,12 @@
 //   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
 //              last PV lands and write O/l or the split partial, while the
 //              softmax warps go on with the next segment.
-// After the pipeline, a grid-wide barrier and a merge phase in which every warp
-// of the grid merges (request, head) pairs of the requests cut into splits.
+// After the pipeline, when some request was cut into splits, a grid-wide
+// barrier and a merge phase in which the grid merges (request, head) pairs of
+// those requests (a warp per pair, or a CTA per pair when pairs are fewer than
+// CTAs).  A launch given the step's new K/V rows stores them first (every
+// thread of the grid a share) and meets at a grid-wide counter before any
+// cache read.
 // Every wait is bounded; the softmax warps take every stop decision at a
 // barrier that reduces it over all four warps, so none is left at a barrier.
 #pragma once
