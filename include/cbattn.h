@@ -108,8 +108,13 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
  * physical block of all heads per MMA tile; the merge runs on the whole grid
  * after a grid-wide barrier, so that launch is cooperative and fails with
  * CB_ECUDA if the device cannot hold one CTA on every SM at once), otherwise on
- * CUDA cores.  Everything is one kernel launch (plus a memset of the
- * workspace's counters).
+ * CUDA cores.  Everything is one kernel launch (plus, except on the block-tile
+ * paths, a memset of the workspace's counters).  The block-tile launches keep
+ * four work counters in library memory instead, one slot per (device, stream)
+ * of 1024 handed out in order of first use, and leave them at zero: calls on
+ * one stream are ordered; calls that overlap on the GPU (unordered streams,
+ * concurrent replays of one captured graph) must come from different streams
+ * holding different slots.
  *
  *  q              device, bf16 [n_tokens][n_q_heads][head_dim]
  *  cu_q_lens      device, int32 [n_reqs + 1], cu_q_lens[0] = 0, non-decreasing,
@@ -192,7 +197,8 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
  *    first call before any stream capture.
  *  - The counters that must start at zero are cleared by every call (an async
- *    memset on `stream`); the partial results are fully rewritten.
+ *    memset on `stream`) or, on the block-tile paths, kept at zero in the
+ *    library's per-stream slots; the partial results are fully rewritten.
  *  - All calls on a device share the one array and it keeps the last call's
  *    contents: calls that may overlap on the GPU (different streams without
  *    ordering between them) race and give undefined results.  Serialise them,

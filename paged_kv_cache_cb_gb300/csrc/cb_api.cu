@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "../../include/cbattn.h"
@@ -12,6 +13,13 @@
 namespace cb {
 
 __device__ unsigned int g_dev_error = 0;
+
+// The block-tile launches' four work counters (chunk claims, merge barrier,
+// append barrier, exits), one slot per (device, stream): zero at load, and
+// every launch leaves its slot at zero (its last CTA resets it), so no launch
+// needs a memset first.
+constexpr int kQueueSlots = 1024;
+__device__ int g_bt_queue[kQueueSlots][4];
 
 namespace {
 
@@ -40,6 +48,23 @@ bool device_info(DeviceInfo* out) {
   }
   *out = d;
   return true;
+}
+
+// Device address of the counter slot of (current device, stream); slots are
+// handed out in order of first use and reused after kQueueSlots streams.
+int* queue_slot(cudaStream_t stream) {
+  static void* base[kMaxDevices] = {};
+  static int next[kMaxDevices] = {};
+  static std::map<std::pair<int, uintptr_t>, int> slot_of;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[dev] && cudaGetSymbolAddress(&base[dev], g_bt_queue) != cudaSuccess) return nullptr;
+  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  auto it = slot_of.find(key);
+  if (it == slot_of.end()) it = slot_of.emplace(key, next[dev]++ % kQueueSlots).first;
+  return static_cast<int*>(base[dev]) + 4 * it->second;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -340,8 +365,13 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
       return CB_ECUDA;
     launches = 2;
   }
-  // split arrival counters and the work queue start at zero every call
-  if (cudaMemsetAsync(ws + L.counters, 0, L.pre_part - L.counters, s) != cudaSuccess) return CB_ECUDA;
+  if (block_tiles) {
+    // library counters that every block-tile launch leaves at zero: no memset
+    p.queue = queue_slot(s);
+    if (!p.queue) return CB_ECUDA;
+  } else if (cudaMemsetAsync(ws + L.counters, 0, L.pre_part - L.counters, s) != cudaSuccess) {
+    return CB_ECUDA;                          // split arrival counters and the work queue start at zero
+  }
   cudaError_t e;
   if (max_q_len == 1 && block_tiles) {
     e = launch_decode_tcb(p, ap, maps[3], maps[4], maps[5], group, std::min(di.n_sms, kMaxDecodeGrid), s);

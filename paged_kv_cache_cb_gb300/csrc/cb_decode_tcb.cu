@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, Cfg<G>::TM);
   }
   merge_phase<G>(P, C, slot, reinterpret_cast<float*>(&T.k[0][0][0][0]));   // the K ring is free now
+  release_counters(P);
 }
 
 template <int G>

@@ -834,6 +834,23 @@ __device__ __forceinline__ void append_wait(const StepParams& P, const AppendPar
   fence_proxy_async_global();
 }
 
+// The launch's counters P.queue[0..3] are left at zero for the next launch on
+// the stream: each CTA counts its exit in P.queue[3] once it is done with all
+// of them, and the last one resets them.  All threads of the CTA call it last.
+__device__ __forceinline__ void release_counters(const StepParams& P) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.queue + 3, 1) == (int)gridDim.x - 1) {
+      P.queue[0] = 0;
+      P.queue[1] = 0;
+      P.queue[2] = 0;
+      __threadfence();
+      P.queue[3] = 0;
+    }
+  }
+}
+
 // After the pipeline, when some request was cut into several splits (every CTA
 // made the same plan, so all take the same branch): a grid-wide barrier (the
 // launch is cooperative, so every CTA is resident; the wait is bounded; the

@@ -851,6 +851,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     }
     tcb::merge_phase<G>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
     if (C.pc_balanced && C2.merge_ok) prefill_merge<A, G>(P, Sp, C, pre);
+    tcb::release_counters(P);
   } else {
     if (warp == 9) {
       tc_fence_after();
