@@ -134,3 +134,21 @@ def test_cpp_scheduler_rejects_bad_prefix():
     s.add_request(0, 20, 2, 1, 5)
     with pytest.raises(L.CBError):
         s.add_request(0, 20, 2, 1, 6)           # one prefix length per group
+
+
+def test_scheduler_memory_and_copies_argument_checks():
+    import ctypes
+    L = _L()
+    lib = L.lib()
+    s = L.Scheduler(8, 16, 32, 4, list(range(8)), 4)
+    out = np.zeros(4, np.int64)
+    assert lib.cb_sched_kv_memory(s._h, 0, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))) == L.CB_EINVAL
+    assert lib.cb_sched_kv_memory(None, 10, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))) == L.CB_EINVAL
+    assert lib.cb_sched_step_copies(s._h, None, -1) == L.CB_EINVAL
+    assert lib.cb_sched_step_copies(s._h, None, 0) == 0          # no step yet: no copies
+    s.add_request(0, 20, 2, 0, 18)
+    s.add_request(1, 20, 2, 0, 18)
+    s.step()
+    s.step()                                                      # the second request takes a copy of the partial block
+    assert s.step_copies().shape == (1, 2)
+    assert lib.cb_sched_step_copies(s._h, None, 0) == L.CB_ESTATE   # one pair does not fit in zero
