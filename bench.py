@@ -541,6 +541,14 @@ def run_trace(args, world, rank, local):
     d_pairs = torch.zeros((budget, 2), dtype=torch.int32, device=dev)
     for hb in h:
         hb["pairs"] = torch.zeros((budget, 2), dtype=torch.int32).pin_memory()
+    # The per-layer step goes straight to the C ABI with pointers taken once, as
+    # a native serving loop would call it: every buffer below keeps its address,
+    # and a step uses the first t rows / b requests of each.
+    step_fn = L.lib().cb_kv_append_paged_attention
+    layer_ptrs = [(kn[i].data_ptr(), vn[i].data_ptr(), qn[i].data_ptr(), kc[i].data_ptr(), vc[i].data_ptr())
+                  for i in range(nl)]
+    fixed = dict(sl=d_sl.data_ptr(), cu=d_cu.data_ptr(), ctx=d_ctx.data_ptr(), bt=d_bt.data_ptr(),
+                 out=out.data_ptr(), ws=ws.data_ptr(), wsb=ws.numel())
 
     def one_step(i, host_io=None):
         m = sched.step()
@@ -579,9 +587,11 @@ def run_trace(args, world, rank, local):
             if npairs:
                 L.cb_copy_blocks(d_pairs[:npairs], kc[layer], vc[layer], sh)
                 stats["launches"] += 1
-            L.cb_kv_append_paged_attention(kn[layer][:t], vn[layer][:t], d_sl[:t], qn[layer][:t], d_cu[:b + 1],
-                                           d_ctx[:b], d_bt[:b], kc[layer], vc[layer], out[:t], scale, ws, max_q,
-                                           max_kv, sh)
+            pk, pv, pq, pkc, pvc = layer_ptrs[layer]
+            rc = step_fn(pk, pv, fixed["sl"], pq, fixed["cu"], fixed["ctx"], fixed["bt"], maxblk, b, t, max_q, max_kv,
+                         pkc, pvc, nb, fixed["out"], scale, hq, hk, a, bs, fixed["ws"], fixed["wsb"], sh)
+            if rc != 0:
+                raise RuntimeError("cb_kv_append_paged_attention: " + L.cb_strerror(rc))
             stats["launches"] += L.cb_last_launch_count()
             if host_io is not None:
                 host_io["out"][:t].copy_(out[:t], non_blocking=True)
