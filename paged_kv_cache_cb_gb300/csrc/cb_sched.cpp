@@ -73,6 +73,7 @@ struct Sched {
   std::vector<int> ref;                // holders of each block
   std::map<int, Prefix> prefixes;      // group -> published prefix
   std::vector<int> copies;             // this step's copy-on-write pairs (src, dst)
+  std::map<int, int> group_prefix;     // prefix length of each group seen
   int n_published = 0;
   std::vector<Req> reqs;
   size_t next_pending = 0;
@@ -188,8 +189,11 @@ int cb_sched_add_request_prefix(cb_sched* h, int arrival_step, int prompt_len, i
     return CB_EINVAL;
   Sched& s = h->s;
   if (!s.reqs.empty() && arrival_step < s.reqs.back().arrival) return CB_EINVAL;
-  for (const Req& o : s.reqs)          // one prefix length per group
-    if (group >= 0 && o.group == group && o.prefix != prefix_len) return CB_EINVAL;
+  if (group >= 0) {                    // one prefix length per group
+    auto it = s.group_prefix.find(group);
+    if (it != s.group_prefix.end() && it->second != prefix_len) return CB_EINVAL;
+    s.group_prefix[group] = prefix_len;
+  }
   Req r;
   r.rid = (int)s.reqs.size();
   r.arrival = arrival_step;
