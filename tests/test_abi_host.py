@@ -124,3 +124,27 @@ def test_host_slot_mapping_rejects_short_tables():
         L.cb_build_slot_mapping([3], [30], np.array([[1, 2]], np.int32), 16)   # needs 3 blocks
     with pytest.raises(L.CBError):
         L.cb_build_slot_mapping([1], [0], np.array([[-1]], np.int32), 16)
+
+
+def test_binding_refuses_host_tensors():
+    """No CPU fallback: every compute entry point of the binding refuses tensors
+    that are not on a CUDA device before anything reaches the library."""
+    import torch
+    L = _lib()
+    bf = torch.bfloat16
+    q = torch.zeros(3, 4, 64, dtype=bf)
+    kn = torch.zeros(3, 4, 64, dtype=bf)
+    sl = torch.zeros(3, dtype=torch.int64)
+    cu = torch.tensor([0, 3], dtype=torch.int32)
+    ctx = torch.tensor([5], dtype=torch.int32)
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    kc = torch.zeros(8, 4, 16, 64, dtype=bf)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.cb_kv_append(kn, kn, sl, kc, kc)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.cb_paged_attention(q, cu, ctx, bt, kc, kc, q.clone(), 0.125, ws, 3, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.cb_kv_append_paged_attention(kn, kn, sl, q, cu, ctx, bt, kc, kc, q.clone(), 0.125, ws, 3, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.cb_copy_blocks(torch.zeros(1, 2, dtype=torch.int32), kc, kc)
