@@ -114,7 +114,9 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
  * of 1024 handed out in order of first use, and leave them at zero: calls on
  * one stream are ordered; calls that overlap on the GPU (unordered streams,
  * concurrent replays of one captured graph) must come from different streams
- * holding different slots.
+ * holding different slots.  The first such call on a device looks up the
+ * array's device address (cudaGetSymbolAddress): make it before any stream
+ * capture.
  *
  *  q              device, bf16 [n_tokens][n_q_heads][head_dim]
  *  cu_q_lens      device, int32 [n_reqs + 1], cu_q_lens[0] = 0, non-decreasing,
