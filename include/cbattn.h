@@ -289,8 +289,8 @@ int cb_sched_add_request(cb_sched* s, int arrival_step, int prompt_len, int outp
  *    prefix holds them);
  *  - a request of the group admitted with nothing stored starts with the
  *    published positions stored: whole blocks shared, a partial last block
- *    copied first into a block of its own (copy-on-write), or, with no free
- *    block for the copy, whole blocks only;
+ *    copied first into a block of its own (copy-on-write); with no block free
+ *    for that copy it waits, like any request that finds no room;
  *  - a running request that needs a block when none is free first drops
  *    published prefixes, oldest first, and only then preempts.
  * Returns the id or CB_EINVAL. */

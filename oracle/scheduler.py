@@ -66,10 +66,11 @@ pages leave these points open):
    - admitting a request of the group with nothing stored: it holds the
      published whole blocks, and a partial last block is copied into a fresh
      block of its own (copy-on-write, listed in the step's metadata for the
-     device to run before the append); with no free block for that copy only
-     whole blocks are shared.  It starts with the shared positions stored.  Its
-     first chunk is min(prompt + produced - shared, budget left, positions
-     that fit: the free blocks after the copy plus the room left in the copy);
+     device to run before the append).  It starts with the shared positions
+     stored.  Its first chunk is min(prompt + produced - shared, budget left,
+     positions that fit: the free blocks after the copy plus the room left in
+     the copy), so with no free block for the copy it is not admitted yet, like
+     any request that finds no room;
    - a running request needing a block when none is free first drops the
      oldest published prefix (repeatedly) and only then preempts; admission
      neither drops prefixes nor preempts.
@@ -283,8 +284,6 @@ class FCFSScheduler:
             pub = self.published.get(req.group) if req.stored == 0 and req.group >= 0 else None
             shared = pub[1] if pub else 0
             tail = shared % self.bs                 # positions in a partial last shared block
-            if tail and not self.free:
-                shared, tail = shared - tail, 0     # no block for the copy: whole blocks only
             room = (len(self.free) - (1 if tail else 0)) * self.bs + (self.bs - tail if tail else 0)
             n = min(req.prompt_len + req.produced - shared, budget, room)
             if n <= 0:

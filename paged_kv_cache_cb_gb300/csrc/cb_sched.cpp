@@ -34,8 +34,9 @@
 //     blocks: whole blocks by reference; a last, partial block is copied into a
 //     block of its own first (copy-on-write: the request will write its own
 //     tokens into that block), the copy listed for the caller to run before the
-//     step's append; with no free block for the copy it shares whole blocks
-//     only.  It starts with the shared positions stored;
+//     step's append (with no block free for the copy it is not admitted yet,
+//     like any request that finds no room).  It starts with the shared
+//     positions stored;
 //  g. when a running request needs a block and none is free, published
 //     prefixes are dropped (oldest first) before a request is preempted.
 // The request that published a prefix keeps writing its own positions into
@@ -336,12 +337,8 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
       auto it = s.prefixes.find(r.group);
       if (it != s.prefixes.end()) px = &it->second;
     }
-    int share = px ? px->tokens : 0;
-    bool cow = share % s.bs != 0;
-    if (cow && s.free_list.empty()) {
-      share -= share % s.bs;
-      cow = false;
-    }
+    const int share = px ? px->tokens : 0;
+    const bool cow = share % s.bs != 0;   // with no block free for the copy, fit <= 0: it waits
     const long long fit =
         (long long)((int)s.free_list.size() - (cow ? 1 : 0)) * s.bs + (cow ? s.bs - share % s.bs : 0);
     const int n = (int)std::min<long long>(std::min(r.prompt + r.produced - share, budget), fit);

@@ -17,9 +17,9 @@ def _L():
     return L
 
 
-def _compare(tr, max_batch=None, max_steps=200000):
+def _compare(tr, max_batch=None, max_steps=200000, free=None):
     L = _L()
-    free = wl.free_order(tr.num_blocks, tr.seed)
+    free = wl.free_order(tr.num_blocks, tr.seed) if free is None else free
     o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free, max_batch=max_batch)
     maxblk = max(-(-(t[1] + t[2] - 1) // tr.block_size) for t in tr.requests)
     mb = max_batch or tr.token_budget
@@ -73,6 +73,26 @@ def test_cpp_scheduler_preempts_like_the_oracle():
 @pytest.mark.parametrize("max_batch", [2, 5])
 def test_cpp_scheduler_batch_cap(max_batch):
     _compare(wl.small_trace(3), max_batch=max_batch)
+
+
+class _Hand:
+    def __init__(self, requests, token_budget, block_size, num_blocks):
+        self.requests, self.token_budget, self.block_size, self.num_blocks = requests, token_budget, block_size, num_blocks
+        self.seed = 0
+
+
+@pytest.mark.parametrize("case", ["batch_cap", "oldest_prefix_dropped", "copy_waits_for_a_block"])
+def test_cpp_scheduler_on_the_hand_worked_cases(case):
+    """The hand-worked scheduler cases of the oracle's pins (request cap, oldest
+    prefix dropped first, a copy-on-write admission waiting for a free block),
+    with their explicit free-list order."""
+    if case == "batch_cap":
+        _compare(_Hand([(0, 4, 3)] * 4, 64, 16, 8), max_batch=2, free=list(range(8)))
+    elif case == "oldest_prefix_dropped":
+        _compare(_Hand([(0, 5, 1, 0, 4), (1, 5, 1, 1, 4), (2, 16, 2), (4, 6, 1, 1, 4)], 64, 4, 6),
+                 free=list(range(6)))
+    else:
+        _compare(_Hand([(0, 7, 2, 0, 6), (0, 7, 2), (1, 7, 1, 0, 6)], 64, 4, 4), free=list(range(4)))
 
 
 def test_cpp_scheduler_full_trace_prefix():

@@ -234,3 +234,72 @@ def test_prefix_sharing_invariants(seed):
                 assert m.ctx_lens[i] == n
                 shares += 1
     assert shares > 0 or all(p[1] % tr.block_size == 0 for p in before.values())
+
+
+def test_max_batch_caps_every_pass():
+    """The optional per-step request cap: four 4-token prompts with 3 outputs
+    each arrive together, the token budget (64) would take them all, and a cap
+    of 2 runs them two at a time -- requests 0 and 1 for their prefill and both
+    decodes, then requests 2 and 3.  Admitting max_batch + 1 (or one fewer)
+    changes the first step's batch."""
+    s = FCFSScheduler([(0, 4, 3)] * 4, token_budget=64, block_size=16, num_blocks=8, free_order=range(8),
+                      max_batch=2)
+    batches = [m.req_ids.tolist() for m in s.run()]
+    assert batches == [[0, 1]] * 3 + [[2, 3]] * 3
+    # without the cap the same requests run together
+    s = FCFSScheduler([(0, 4, 3)] * 4, token_budget=64, block_size=16, num_blocks=8, free_order=range(8))
+    assert [m.req_ids.tolist() for m in s.run()] == [[0, 1, 2, 3]] * 3
+
+
+def _two_prefixes_then_pressure():
+    """Blocks of 4, a pool of 6.  Request 0 (group 0) and request 1 (group 1)
+    each store a 4-token prefix in one block, publish it and finish, so that
+    only the published prefixes hold blocks 0 and 2.  Request 2 (no group)
+    then takes the four free blocks with a 16-token prompt, and its first
+    decode (position 16) needs a fifth block while none is free."""
+    reqs = [(0, 5, 1, 0, 4), (1, 5, 1, 1, 4), (2, 16, 2), (4, 6, 1, 1, 4)]
+    return FCFSScheduler(reqs, token_budget=64, block_size=4, num_blocks=6, free_order=range(6))
+
+
+def test_prefix_drop_takes_the_oldest_first():
+    """A running request short of a block first drops published prefixes,
+    oldest publication first ([KVN] §与Prefix Caching的结合 gives the sharing;
+    the order is this scheduler's reading).  Group 0's prefix (block 0,
+    published first) goes; group 1's (block 2) stays and is shared by the
+    group-1 request that arrives later.  Dropping the newest would hand block 2
+    to request 2 instead; preempting instead of dropping would stop request 2."""
+    s = _two_prefixes_then_pressure()
+    m0, m1, m2 = s.step(), s.step(), s.step()
+    assert m0.block_tables == [[0, 1]] and m1.block_tables == [[2, 3]]
+    assert sorted(s.published) == [0, 1] and s.published[0][0] == [0] and s.published[1][0] == [2]
+    assert m2.block_tables == [[4, 5, 1, 3]] and len(s.free) == 0
+    m3 = s.step()                                  # request 2 decodes position 16
+    assert m3.req_ids.tolist() == [2] and m3.preempted == []
+    assert m3.block_tables == [[4, 5, 1, 3, 0]]    # block 0: group 0's prefix, dropped
+    assert list(s.published) == [1] and s.published[1][0] == [2]
+    m4 = s.step()                                  # request 3 (group 1) joins the surviving prefix
+    assert m4.req_ids.tolist() == [3] and m4.ctx_lens.tolist() == [4] and m4.q_lens.tolist() == [2]
+    assert m4.block_tables[0][0] == 2 and m4.copies == []
+
+
+def test_partial_prefix_block_waits_for_a_free_block():
+    """Copy-on-write needs a block for the copy: a request joining a prefix
+    whose last block is partial is not admitted while no block is free (no
+    copy is listed and nothing is shared yet), and is admitted with the copy as
+    soon as one is.  Blocks of 4, a pool of 4: requests 0 and 1 (7-token
+    prompts, 2 outputs: 8 positions, two blocks each) fill the pool; request 0
+    publishes its 6-token prefix (blocks 0 and 1, block 1 partial).  Request 2
+    of the same group arrives at step 1, while no block is free."""
+    reqs = [(0, 7, 2, 0, 6), (0, 7, 2), (1, 7, 1, 0, 6)]
+    s = FCFSScheduler(reqs, token_budget=64, block_size=4, num_blocks=4, free_order=range(4))
+    m0 = s.step()
+    assert m0.req_ids.tolist() == [0, 1] and m0.block_tables == [[0, 1], [2, 3]] and len(s.free) == 0
+    assert s.published[0][:2] == ([0, 1], 6)
+    m1 = s.step()                  # both decode their last token; request 2 cannot be admitted
+    assert m1.req_ids.tolist() == [0, 1] and m1.copies == [] and m1.preempted == []
+    assert s.reqs[2].state == "waiting" and s.reqs[2].blocks == []
+    assert s.holders[:2] == [1, 1] and sorted(s.free) == [2, 3]   # the prefix alone holds blocks 0, 1
+    m2 = s.step()                  # block 2 is free: whole block 0 shared, partial block 1 copied into 2
+    assert m2.req_ids.tolist() == [2] and m2.copies == [(1, 2)]
+    assert m2.block_tables == [[0, 2]] and m2.ctx_lens.tolist() == [6] and m2.q_lens.tolist() == [1]
+    assert m2.slot_mapping.tolist() == [2 * 4 + 6 % 4]
