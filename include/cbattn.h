@@ -37,6 +37,15 @@
  *  - Return value: CB_OK (0) on success, a negative CB_E* code otherwise.  Size
  *    and pointer checks happen on the host before anything is enqueued; a
  *    rejected call enqueues nothing.
+ *  - Per-stream state: the library keeps, in its own device memory, one slot
+ *    per (device, stream) used -- an error word that the kernels launched on
+ *    that stream report bad metadata or timeouts into (read and cleared by
+ *    cb_last_error(stream)), and the block-tile launches' work counters.  Slots
+ *    are handed out in order of first use, at most 4096 per device; a call on a
+ *    further stream returns CB_ESTATE.  The first call on a device looks up the
+ *    slots' device address (cudaGetSymbolAddress): make it before any stream
+ *    capture.  Addresses are cached per device, so cudaDeviceReset is not
+ *    supported while the library is in use.
  */
 #ifndef CBATTN_H
 #define CBATTN_H
@@ -110,13 +119,10 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
  * CB_ECUDA if the device cannot hold one CTA on every SM at once), otherwise on
  * CUDA cores.  Everything is one kernel launch (plus, except on the block-tile
  * paths, a memset of the workspace's counters).  The block-tile launches keep
- * four work counters in library memory instead, one slot per (device, stream)
- * of 1024 handed out in order of first use, and leave them at zero: calls on
- * one stream are ordered; calls that overlap on the GPU (unordered streams,
- * concurrent replays of one captured graph) must come from different streams
- * holding different slots.  The first such call on a device looks up the
- * array's device address (cudaGetSymbolAddress): make it before any stream
- * capture.
+ * four work counters in the stream's library slot instead (see "Per-stream
+ * state" above) and leave them at zero: calls on one stream are ordered; calls
+ * that overlap on the GPU (unordered streams, concurrent replays of one
+ * captured graph) must come from different streams.
  *
  *  q              device, bf16 [n_tokens][n_q_heads][head_dim]
  *  cu_q_lens      device, int32 [n_reqs + 1], cu_q_lens[0] = 0, non-decreasing,
@@ -192,9 +198,13 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
  * library-owned device array of CB_NOALLOC_SCRATCH_BYTES, held on every GPU that
  * loads the library until the process exits.  Nothing is allocated per call.
  *  - Sizes whose smallest accepted workspace exceeds CB_NOALLOC_SCRATCH_BYTES
- *    are rejected with CB_EWORKSPACE before anything is enqueued (without room
- *    for the balanced prefill's partial results the launch keeps prefill tile
- *    pairs whole).
+ *    are rejected with CB_EWORKSPACE before anything is enqueued.
+ *  - It uses as much of the array as cb_paged_attention_workspace_size asks
+ *    for, so a step whose full workspace fits is planned exactly as
+ *    cb_paged_attention plans it with that workspace (the same outputs, bit
+ *    for bit).  A larger step is run with the array alone: without room for
+ *    the balanced prefill's partial results the launch keeps prefill tile
+ *    pairs whole, and its outputs then differ within rounding.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
  *    first call before any stream capture.
@@ -214,7 +224,9 @@ int cb_paged_attention_noalloc(const void* q, const int32_t* cu_q_lens, const in
                                int num_blocks, void* out, float scale, int n_q_heads, int n_kv_heads,
                                int head_dim, int block_size, void* stream);
 
-/* Synchronise `stream`, then read and clear the device error word.
+/* Synchronise `stream`, then read and clear that stream's error word: the bad
+ * metadata or timeouts reported by kernels this library launched on `stream`
+ * (never another stream's).
  * Returns CB_OK, CB_EDEVICE, CB_ETIMEOUT or CB_ECUDA. */
 int cb_last_error(void* stream);
 
@@ -226,15 +238,8 @@ const char* cb_strerror(int code);
  * aligned) with a plain streaming kernel: the HBM copy roofline probe. */
 int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream);
 
-/* Diagnostic: out[i] = 2^t[i] computed on the device by the polynomial that the
- * prefill softmax uses for part of its probabilities (FMA pipe instead of the
- * special-function unit).  t, out: device float arrays of n elements, n even.
- * Relative error below 1e-4 for -125 <= t <= 127; inputs below -125 give 2^-125.
- * Returns CB_OK, CB_EINVAL (odd n, null pointer) or CB_ECUDA. */
-int cb_exp2_poly(const float* t, float* out, int n, void* stream);
-
-/* Number of kernels the last successful cb_paged_attention / cb_kv_append call
- * enqueued (for launch accounting in benchmarks). */
+/* Number of kernels the calling thread's last successful GPU call of this
+ * library enqueued (for launch accounting in benchmarks). */
 int cb_last_launch_count(void);
 
 /* ---------------------------------------------------------------- host metadata

@@ -38,7 +38,6 @@ SIGNATURES = [
     ("cb_strerror", ctypes.c_char_p, [_c_int]),
     ("cb_hbm_copy", _c_int, [_vp, _vp, _c_size, _vp]),
     ("cb_last_launch_count", _c_int, []),
-    ("cb_exp2_poly", _c_int, [_vp, _vp, _c_int, _vp]),
     ("cb_build_slot_mapping", _c_int, [_i32p, _i32p, _i32p, _c_int, _c_int, _c_int, _i64p]),
     ("cb_sched_create", _vp, [_c_int, _c_int, _c_int, _c_int, _i32p]),
     ("cb_sched_destroy", None, [_vp]),
@@ -254,7 +253,7 @@ def cb_paged_attention_noalloc(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_
 
 
 def cb_last_error(stream=None):
-    """Synchronise the stream and return (and clear) the device error status code."""
+    """Synchronise the stream and return (and clear) that stream's error status code."""
     return int(lib().cb_last_error(_stream(stream)))
 
 
@@ -268,16 +267,6 @@ def cb_hbm_copy(dst, src, stream=None):
         raise ValueError("bad copy buffers")
     _check("cb_hbm_copy", lib().cb_hbm_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), n,
                                             _stream(stream)))
-
-
-def cb_exp2_poly(t, out, stream=None):
-    """out = 2^t by the prefill softmax's FMA-pipe polynomial (float32 CUDA tensors)."""
-    import torch
-    pt = _dev(t, torch.float32, "t")
-    po = _dev(out, torch.float32, "out")
-    if out.numel() != t.numel():
-        raise ValueError("shape mismatch")
-    _check("cb_exp2_poly", lib().cb_exp2_poly(pt, po, t.numel(), _stream(stream)))
 
 
 def cb_last_launch_count():

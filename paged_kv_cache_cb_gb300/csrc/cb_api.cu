@@ -1,34 +1,39 @@
 // C-ABI entry points of include/cbattn.h: argument checks, workspace carving,
-// TMA tensor-map encoding and kernel dispatch.  Host code only (plus the device
-// error word).
+// TMA tensor-map encoding and kernel dispatch.  Host code only (plus the
+// library's per-stream device state).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <set>
 
 #include "../../include/cbattn.h"
 #include "cb_internal.h"
 
 namespace cb {
 
-__device__ unsigned int g_dev_error = 0;
-
-// The block-tile launches' four work counters (chunk claims, merge barrier,
-// append barrier, exits), one slot per (device, stream): zero at load, and
-// every launch leaves its slot at zero (its last CTA resets it), so no launch
-// needs a memset first.
-constexpr int kQueueSlots = 1024;
-__device__ int g_bt_queue[kQueueSlots][4];
+// Library state of one (device, stream): the block-tile launches' four work
+// counters (chunk claims, merge barrier, append barrier, exits) and the error
+// word that every kernel launched on that stream ORs its CB_DEVERR_* bits into.
+// Zero at load; every block-tile launch leaves its counters at zero (its last
+// CTA resets them), so no launch needs a memset first; cb_last_error(stream)
+// reads and clears the stream's error word.
+struct StreamSlot {
+  int queue[4];
+  unsigned int err;
+  unsigned int pad[3];
+};
+constexpr int kStreamSlots = 4096;
+__device__ StreamSlot g_stream_slots[kStreamSlots];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_last_launches = 0;
+thread_local int g_last_launches = 0;
 
 struct DeviceInfo {
   int n_sms = 0;
-  unsigned int* err = nullptr;
 };
 
 bool device_info(DeviceInfo* out) {
@@ -41,30 +46,46 @@ bool device_info(DeviceInfo* out) {
   if (d.n_sms == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return false;
-    d.err = static_cast<unsigned int*>(p);
     d.n_sms = sms;
   }
   *out = d;
   return true;
 }
 
-// Device address of the counter slot of (current device, stream); slots are
-// handed out in order of first use and reused after kQueueSlots streams.
-int* queue_slot(cudaStream_t stream) {
+// The slot of (current device, stream), handed out in order of first use
+// (create = false: only look it up).  Returns nullptr on a CUDA error, when a
+// device has used up its kStreamSlots slots (*full = true), or, without
+// create, when the stream has none yet.
+StreamSlot* stream_slot(cudaStream_t stream, bool create, bool* full = nullptr) {
   static void* base[kMaxDevices] = {};
   static int next[kMaxDevices] = {};
   static std::map<std::pair<int, uintptr_t>, int> slot_of;
   static std::mutex mu;
+  if (full) *full = false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!base[dev] && cudaGetSymbolAddress(&base[dev], g_bt_queue) != cudaSuccess) return nullptr;
+  if (!base[dev] && cudaGetSymbolAddress(&base[dev], g_stream_slots) != cudaSuccess) return nullptr;
   const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
   auto it = slot_of.find(key);
-  if (it == slot_of.end()) it = slot_of.emplace(key, next[dev]++ % kQueueSlots).first;
-  return static_cast<int*>(base[dev]) + 4 * it->second;
+  if (it == slot_of.end()) {
+    if (!create) return nullptr;
+    if (next[dev] >= kStreamSlots) {
+      if (full) *full = true;
+      return nullptr;
+    }
+    it = slot_of.emplace(key, next[dev]++).first;
+  }
+  return static_cast<StreamSlot*>(base[dev]) + it->second;
+}
+
+// Error word of `stream`'s slot for a launch (nullptr: see stream_slot); rc
+// receives the code to return when there is none.
+unsigned int* launch_err(cudaStream_t stream, int* rc) {
+  bool full = false;
+  StreamSlot* sl = stream_slot(stream, true, &full);
+  *rc = full ? CB_ESTATE : CB_ECUDA;
+  return sl ? &sl->err : nullptr;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -121,6 +142,21 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Smallest decode split the launcher may choose; the workspace is sized for it.
 constexpr int kMinSplitBlocks = 8;
+
+// The dynamic shared-memory opt-in of a kernel, once per (device, kernel): the
+// attribute belongs to the current device's context.
+cudaError_t opt_in_smem(const void* kernel, int bytes) {
+  static std::set<std::pair<int, const void*>> done;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, kernel})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({dev, kernel});
+  return e;
+}
 
 namespace {
 
@@ -213,10 +249,11 @@ int cb_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mappi
   }
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return CB_EINVAL;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache)) return CB_EINVAL;
-  DeviceInfo di;
-  if (!device_info(&di)) return CB_ECUDA;
+  int rc = CB_OK;
+  unsigned int* err = launch_err(static_cast<cudaStream_t>(stream), &rc);
+  if (!err) return rc;
   cudaError_t e = launch_kv_append(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_blocks, n_kv_heads,
-                                   head_dim, di.err, static_cast<cudaStream_t>(stream));
+                                   head_dim, err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return CB_ECUDA;
   g_last_launches = 1;
   return CB_OK;
@@ -232,9 +269,10 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
     return CB_OK;
   }
   if (!pairs || !k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return CB_EINVAL;
-  DeviceInfo di;
-  if (!device_info(&di)) return CB_ECUDA;
-  if (launch_copy_blocks(pairs, n_pairs, k_cache, v_cache, num_blocks, n_kv_heads, head_dim, di.err,
+  int rc = CB_OK;
+  unsigned int* err = launch_err(static_cast<cudaStream_t>(stream), &rc);
+  if (!err) return rc;
+  if (launch_copy_blocks(pairs, n_pairs, k_cache, v_cache, num_blocks, n_kv_heads, head_dim, err,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CB_ECUDA;
   g_last_launches = 1;
@@ -298,13 +336,18 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
   if (app && (!app->k_new || !app->v_new || !app->slots || !aligned16(app->k_new) || !aligned16(app->v_new)))
     return CB_EINVAL;
   // the balanced prefill's partial results when the workspace has room for them
-  WorkspaceLayout L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8, max_q_len > 1);
-  if (workspace_bytes < L0.total) L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, 8, false);
+  WorkspaceLayout L0 =
+      workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks, max_q_len > 1);
+  if (workspace_bytes < L0.total)
+    L0 = workspace_layout(n_reqs, max_kv_len, n_q_heads, n_kv_heads, head_dim, kMinSplitBlocks, false);
   if (workspace_bytes < L0.total) return CB_EWORKSPACE;
   const WorkspaceLayout L = workspace_layout_for_bytes(L0, workspace_bytes, n_reqs, n_q_heads, n_kv_heads, head_dim);
   DeviceInfo di;
   if (!device_info(&di)) return CB_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool slots_full = false;
+  StreamSlot* slot = stream_slot(s, true, &slots_full);
+  if (!slot) return slots_full ? CB_ESTATE : CB_ECUDA;
 
   StepParams p{};
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -327,7 +370,7 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
   p.queue = reinterpret_cast<int*>(ws + L.queue);
   p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
   p.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
-  p.err = di.err;
+  p.err = &slot->err;
 
   const int group = n_q_heads / n_kv_heads;
   // GQA with 8 KV heads and head_dim 128: decode tokens run the block-tile
@@ -361,14 +404,13 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
     ap.n_tokens = n_tokens;
   } else if (app) {
     if (launch_kv_append(app->k_new, app->v_new, app->slots, n_tokens, const_cast<void*>(k_cache),
-                         const_cast<void*>(v_cache), num_blocks, n_kv_heads, head_dim, di.err, s) != cudaSuccess)
+                         const_cast<void*>(v_cache), num_blocks, n_kv_heads, head_dim, p.err, s) != cudaSuccess)
       return CB_ECUDA;
     launches = 2;
   }
   if (block_tiles) {
     // library counters that every block-tile launch leaves at zero: no memset
-    p.queue = queue_slot(s);
-    if (!p.queue) return CB_ECUDA;
+    p.queue = slot->queue;
   } else if (cudaMemsetAsync(ws + L.counters, 0, L.pre_part - L.counters, s) != cudaSuccess) {
     return CB_ECUDA;                          // split arrival counters and the work queue start at zero
   }
@@ -419,12 +461,15 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
 }
 
 int cb_last_error(void* stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CB_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CB_ECUDA;
+  StreamSlot* slot = stream_slot(s, false);
+  if (!slot) return CB_OK;                       // nothing was launched on this stream
   unsigned int bits = 0;
-  if (cudaMemcpyFromSymbol(&bits, g_dev_error, sizeof(bits)) != cudaSuccess) return CB_ECUDA;
+  if (cudaMemcpy(&bits, &slot->err, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return CB_ECUDA;
   if (bits) {
     const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return CB_ECUDA;
+    if (cudaMemcpy(&slot->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return CB_ECUDA;
   }
   if (bits & CB_DEVERR_TIMEOUT) return CB_ETIMEOUT;
   if (bits) return CB_EDEVICE;
@@ -439,7 +484,7 @@ const char* cb_strerror(int code) {
     case CB_EWORKSPACE: return "workspace too small";
     case CB_EDEVICE: return "kernel found bad metadata (block id, slot or length out of range)";
     case CB_ETIMEOUT: return "kernel wait timed out";
-    case CB_ESTATE: return "scheduler state error or capacity exceeded";
+    case CB_ESTATE: return "state error or capacity exceeded (scheduler, or streams per device)";
     default: return "unknown error";
   }
 }
@@ -454,12 +499,5 @@ int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream) {
 }
 
 int cb_last_launch_count(void) { return g_last_launches; }
-
-int cb_exp2_poly(const float* t, float* out, int n, void* stream) {
-  if (!t || !out || n < 0 || (n & 1)) return CB_EINVAL;
-  if (launch_exp2_poly(t, out, n, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CB_ECUDA;
-  g_last_launches = 1;
-  return CB_OK;
-}
 
 }  // extern "C"

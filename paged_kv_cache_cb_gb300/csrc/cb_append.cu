@@ -93,23 +93,4 @@ cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms,
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- 2^t check
-// Evaluates, pair by pair, the FMA-pipe 2^t that the prefill softmax uses for
-// part of its probabilities, so that tests can hold it against CUDA's exp2.
-__global__ void exp2_poly_kernel(const float* __restrict__ t, float* __restrict__ out, int n_pairs) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_pairs; i += gridDim.x * blockDim.x) {
-    float lo, hi;
-    exp2_poly_pair(f2(t[2 * i], t[2 * i + 1]), lo, hi);
-    out[2 * i] = lo;
-    out[2 * i + 1] = hi;
-  }
-}
-
-cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream) {
-  if (n <= 0) return cudaSuccess;
-  const int pairs = n / 2;
-  exp2_poly_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(t, out, pairs);
-  return cudaGetLastError();
-}
-
 }  // namespace cb

@@ -18,8 +18,9 @@
 namespace cb {
 
 // ---------------------------------------------------------------- error word
-// One word per device (its address reaches kernels as a parameter), OR-ed with
-// CB_DEVERR_* bits by kernels; read and cleared by cb_last_error().
+// One word per (device, stream) in the library's stream slots (its address
+// reaches kernels as a parameter), OR-ed with CB_DEVERR_* bits by kernels; read
+// and cleared by cb_last_error(stream).
 __device__ __forceinline__ void set_error(unsigned int* err, unsigned int bits) { atomicOr(err, bits); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -331,29 +332,6 @@ __device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
-}
-// 2^t for a pair, on the FMA pipe instead of the special-function unit:
-// t = n + f with n = round(t) (added to and subtracted from 1.5 * 2^23, which
-// leaves n in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a cubic fitted
-// for minimum relative error on that interval (max 8.4e-5, far below the bf16
-// rounding of P); 2^n by adding n to the exponent field.  t is clamped at -125
-// so the exponent stays normal (2^-125 is negligible next to the row's largest
-// weight, which is at least 1).  Valid for t <= 127.
-__device__ __forceinline__ void exp2_poly_pair(uint64_t t, float& lo, float& hi) {
-  float t0, t1;
-  f2split(t, t0, t1);
-  const uint64_t tc = f2(fmaxf(t0, -125.f), fmaxf(t1, -125.f));
-  const uint64_t magic = f2(12582912.f, 12582912.f);
-  const uint64_t j = fadd2(tc, magic);
-  const uint64_t fr = fsub2(tc, fsub2(j, magic));
-  uint64_t p = ffma2(f2(0x1.c44e0ap-5f, 0x1.c44e0ap-5f), fr, f2(0x1.f1141cp-3f, 0x1.f1141cp-3f));
-  p = ffma2(p, fr, f2(0x1.62f342p-1f, 0x1.62f342p-1f));
-  p = ffma2(p, fr, f2(0x1.fff576p-1f, 0x1.fff576p-1f));
-  float p0, p1, j0, j1;
-  f2split(p, p0, p1);
-  f2split(j, j0, j1);
-  lo = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(j0) << 23));
-  hi = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(j1) << 23));
 }
 // bf16 pair (packed in a 32-bit word, low half first) -> two floats; exact.
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }

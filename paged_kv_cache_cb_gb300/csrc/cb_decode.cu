@@ -49,12 +49,8 @@ cudaError_t launch_decode_t(const StepParams& p, const CUtensorMap& kmap, const 
                             cudaStream_t stream) {
   using C = DecodeCfg<A, G>;
   const size_t smem = 1024 + C::NW * sizeof(typename C::WS) + (size_t)(2 * (p.n_reqs + 1) + 96) * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<A, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(decode_kernel<A, G>), kSmemLimit);
+  if (e != cudaSuccess) return e;
   decode_kernel<A, G><<<n_sms, C::NW * 32, smem, stream>>>(p, kmap, vmap);
   return cudaGetLastError();
 }

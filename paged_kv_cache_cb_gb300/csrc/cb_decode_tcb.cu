@@ -67,13 +67,8 @@ cudaError_t launch_t(const StepParams& p, const AppendParams& ap, const CUtensor
                      const CUtensorMap& qmap, int n_sms, cudaStream_t stream) {
   const size_t smem = smem_bytes<G>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_tcb_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(decode_tcb_kernel<G>), kSmemLimit);
+  if (e != cudaSuccess) return e;
   // cooperative: the merge phase waits for every CTA
   StepParams pc = p;
   AppendParams apc = ap;

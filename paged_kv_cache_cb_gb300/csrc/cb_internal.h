@@ -46,7 +46,7 @@ struct StepParams {
   int* queue;                   // [4] work counters (zeroed per call)
   float* part_ml;               // [max_splits_total * Hq * 2] (max, sum) per split and head
   float* part_acc;              // [max_splits_total * Hq * A] unnormalised outputs per split
-  unsigned int* err;            // device error word
+  unsigned int* err;            // the launching stream's error word
 };
 
 // The step's new K/V rows when the block-tile launches store them themselves
@@ -87,6 +87,9 @@ size_t workspace_min_bytes(int n_reqs, int n_tokens, int max_q_len, int max_kv_l
 WorkspaceLayout workspace_layout_for_bytes(const WorkspaceLayout& L, size_t bytes, int n_reqs, int n_q_heads,
                                            int n_kv_heads, int head_dim);
 int choose_split_blocks(int n_reqs, int max_kv_len, int n_kv_heads, int n_sms);
+// Dynamic shared-memory opt-in of `kernel` on the current device (set once per
+// device and kernel).
+cudaError_t opt_in_smem(const void* kernel, int bytes);
 
 // Kernel launchers (defined in the .cu files); return a cudaError_t.
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t* slots, int n_tokens,
@@ -109,6 +112,5 @@ cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const Pref
 cudaError_t launch_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cache, int num_blocks,
                                int n_kv_heads, int head_dim, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_hbm_copy(void* dst, const void* src, size_t bytes, int n_sms, cudaStream_t stream);
-cudaError_t launch_exp2_poly(const float* t, float* out, int n, cudaStream_t stream);
 
 }  // namespace cb

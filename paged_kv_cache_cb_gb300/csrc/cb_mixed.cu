@@ -51,13 +51,6 @@ constexpr int kSmemLimit = 232448;
 constexpr int kNumThreads = 320;
 constexpr int kDecWarps = 8;
 constexpr int kDecStages = 2;
-// Of every 16 pairs of scores, pairs kPolyFrom..15 take 2^x from the FMA-pipe
-// polynomial instead of the special-function unit.  16 = off: measured on the
-// long-context chunk, the special-function unit is not the limiter here (the
-// tensor core's cost per 128x128x16 MMA with both operands in shared memory,
-// ~107 cycles, sets the pace), and the polynomial's extra instructions cost
-// 8% (954 vs 875 TFLOP/s with 4 of 16 pairs).
-constexpr int kPolyFrom = 16;
 
 template <int A>
 struct PrefillTiles {
@@ -557,9 +550,7 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
         }
       }
       // pass 2: p = 2^(s*scale*log2 e - m), packed to bf16 pairs over the S columns
-      // (64 columns per load).  Pairs are computed with packed fp32x2 FMA; pairs
-      // kPolyFrom..15 of every 16 take 2^x from the FMA-pipe polynomial to
-      // offload the special-function unit.
+      // (64 columns per load), the exponent arguments with packed fp32x2 FMAs.
       const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
       uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
@@ -571,15 +562,9 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const uint64_t t = ffma2(f2(sv[2 * k], sv[2 * k + 1]), sl2x2, nmx2);
-          float p0, p1;
-          if ((k & 15) >= kPolyFrom) {
-            exp2_poly_pair(t, p0, p1);
-          } else {
-            float t0, t1;
-            f2split(t, t0, t1);
-            p0 = ex2(t0);
-            p1 = ex2(t1);
-          }
+          float t0, t1;
+          f2split(t, t0, t1);
+          float p0 = ex2(t0), p1 = ex2(t1);
           if (masked_tile) {
             const int key = key0 + h * 64 + 2 * k;
             p0 = key > pos ? 0.f : p0;
@@ -871,13 +856,8 @@ cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const Pr
   const size_t smem = mixed_smem<A, G, BT>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
   if (!BT && ap.n_tokens != 0) return cudaErrorInvalidValue;   // only the cooperative launch stores rows
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(mixed_kernel<A, G, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), kSmemLimit);
+  if (e != cudaSuccess) return e;
   if constexpr (BT) {   // cooperative: the decode merge phase waits for every CTA
     StepParams pc = p;
     AppendParams apc = ap;

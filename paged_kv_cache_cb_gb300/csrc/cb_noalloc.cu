@@ -58,7 +58,12 @@ extern "C" int cb_paged_attention_noalloc(const void* q, const int32_t* cu_q_len
   if (need > (size_t)CB_NOALLOC_SCRATCH_BYTES) return CB_EWORKSPACE;   // sizes beyond the fixed scratch
   void* ws = scratch_address();
   if (!ws) return CB_ECUDA;
+  // as much of the array as the size query asks for: the same plan as the
+  // workspace entry point given that workspace, whenever it fits
+  const size_t want = cb_paged_attention_workspace_size(n_reqs, n_tokens, max_q_len, max_kv_len, n_q_heads,
+                                                        n_kv_heads, head_dim, block_size);
+  const size_t use = want < (size_t)CB_NOALLOC_SCRATCH_BYTES ? want : (size_t)CB_NOALLOC_SCRATCH_BYTES;
   return cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens, max_q_len,
                             max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads, head_dim,
-                            block_size, ws, (size_t)CB_NOALLOC_SCRATCH_BYTES, stream);
+                            block_size, ws, use, stream);
 }

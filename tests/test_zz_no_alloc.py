@@ -67,12 +67,20 @@ def test_no_alloc_matches_workspace_entry_point_twice(shape):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     m = _step_buffers(shape)
-    ref = _with_workspace(shape, m).float().cpu().numpy()
+    ref_t = _with_workspace(shape, m)
+    ref = ref_t.float().cpu().numpy()
+    lib = L()
+    fits = lib.cb_paged_attention_workspace_size(shape.n_reqs, shape.n_tokens, m["max_q"], m["max_kv"], shape.n_q_heads,
+                                                 shape.n_kv_heads, shape.head_dim,
+                                                 shape.block_size) <= lib.CB_NOALLOC_SCRATCH_BYTES
     for call in range(2):          # the shared scratch keeps the previous call's contents
-        got = _no_alloc(m).float().cpu().numpy()
+        got_t = _no_alloc(m)
+        got = got_t.float().cpu().numpy()
         assert np.isfinite(got).all(), f"call {call}: non-finite output"
         err = float(np.abs(got - ref).max())
         assert err <= ATOL, f"call {call}: max abs difference {err}"
+        if fits:                   # the same plan as the workspace entry point: the same bits
+            assert torch.equal(got_t, ref_t), f"call {call}: planned differently"
 
 
 def test_no_alloc_rejects_steps_larger_than_its_scratch():
