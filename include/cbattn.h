@@ -33,7 +33,8 @@
  *  - GQA / MQA ([KVN] MQA/GQA): n_q_heads % n_kv_heads == 0 and query head h
  *    reads KV head h / (n_q_heads / n_kv_heads).
  *  - Supported shapes: head_dim 64 or 128; block_size 16;
- *    n_q_heads / n_kv_heads in {1, 2, 4, 8}; n_reqs <= CB_MAX_REQS.
+ *    n_q_heads / n_kv_heads in {1, 2, 4, 8}; with head_dim 128 also 32 query
+ *    heads on 2 KV heads (16 per group) or on 1 (MQA); n_reqs <= CB_MAX_REQS.
  *  - Return value: CB_OK (0) on success, a negative CB_E* code otherwise.  Size
  *    and pointer checks happen on the host before anything is enqueued; a
  *    rejected call enqueues nothing.
@@ -113,8 +114,9 @@ int cb_copy_blocks(const int32_t* pairs, int n_pairs, void* k_cache, void* v_cac
  * never see each other's keys (the block-diagonal ragged mask).
  * Requests with q_len > 1 run as 128-row tiles on the tensor cores.  Decode
  * requests (q_len == 1) are split over their KV blocks and the splits merged by
- * log-sum-exp: with 8 KV heads and head_dim 128 on the tensor cores (one
- * physical block of all heads per MMA tile; the merge runs on the whole grid
+ * log-sum-exp: with head_dim 128 and 8 KV heads (or 32 query heads on 1 or 2)
+ * on the tensor cores (128-row MMA tiles of whole physical blocks of every KV
+ * head: one block of 8 heads, 4 of 2, 8 of 1; the merge runs on the whole grid
  * after a grid-wide barrier, so that launch is cooperative and fails with
  * CB_ECUDA if the device cannot hold one CTA on every SM at once), otherwise on
  * CUDA cores.  Everything is one kernel launch (plus, except on the block-tile
@@ -184,6 +186,35 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
                                  void* v_cache, int num_blocks, void* out, float scale, int n_q_heads,
                                  int n_kv_heads, int head_dim, int block_size, void* workspace,
                                  size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- rolling window
+ * [KVB] "Rolling KV Cache" (a heading whose body is missing from the page).
+ * Reading: a rolling cache keeps each request's W most recent keys, so new
+ * token i of request r (absolute position p = ctx + i) attends to the keys at
+ * positions max(0, p - W + 1) .. p only:
+ *     out[t][h] = softmax_j(scale * q[t][h] . K[j]) . V[j],   p - W < j <= p.
+ * Same arguments, layouts, workspace and errors as cb_paged_attention (and
+ * cb_kv_append_paged_attention), plus
+ *  window   W >= 1 (0: no window, the same as the calls without it; < 0:
+ *           CB_EINVAL).
+ * Decodes read only the blocks from the one holding position ctx + 1 - W on;
+ * prefill tiles skip key tiles that no query of the tile can see.  Block-table
+ * entries before a request's window are never read, so a caller may already
+ * have released those blocks (cb_sched_set_window does) and left any value
+ * there.  The workspace size query is the same. */
+int cb_paged_attention_window(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                              const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                              int max_q_len, int max_kv_len, const void* k_cache, const void* v_cache, int num_blocks,
+                              void* out, float scale, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                              int window, void* workspace, size_t workspace_bytes, void* stream);
+
+int cb_kv_append_paged_attention_window(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                        const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                                        const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                                        int max_q_len, int max_kv_len, void* k_cache, void* v_cache, int num_blocks,
+                                        void* out, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int block_size, int window, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /* ---------------------------------------------------------------- no-allocation variant
  * The pages have no counterpart: this exists for callers that cannot allocate
@@ -277,6 +308,46 @@ cb_sched* cb_sched_create(int num_blocks, int block_size, int token_budget, int 
                           const int32_t* free_order);
 void cb_sched_destroy(cb_sched* s);
 
+/* Padded batching instead of continuous batching -- the baselines of [CB]
+ * Continuous batching (batched generation: prompts padded on the left to the
+ * batch's longest, the batch run until its longest generation ends) and [SM]
+ * 动态批处理 (dynamic batching: the requests that arrive within a waiting window,
+ * or until the batch is full, run as one batch).  From then on cb_sched_step
+ * plans padded batches:
+ *  - a batch forms only when none is running, from the waiting requests in
+ *    arrival order, at most batch_size of them, once batch_size are waiting,
+ *    no further request will arrive, or (max_wait >= 0, dynamic batching) the
+ *    oldest has waited max_wait steps since its arrival; max_wait -1: static
+ *    batching, which waits for a full batch; the batch is cut from its end
+ *    until its padded length fits the pool;
+ *  - its first step is the padded prefill: every request processes n_max
+ *    positions (the longest prompt; the first n_max - prompt_len are pads) at
+ *    ctx 0; then one position per request per step (ctx n_max, n_max + 1, ...)
+ *    until the longest output is done, finished requests decoding pads;
+ *  - blocks are taken on demand and all return when the batch ends; prefix
+ *    groups, preemption and the rolling window do not apply.
+ * The token budget given to cb_sched_create is then only the capacity of the
+ * step's slot_mapping array (a padded prefill needs batch_size x the longest
+ * prompt); a step that does not fit returns CB_ESTATE.
+ * batch_size 1 .. max_batch.  Call before the first cb_sched_step.  Returns
+ * CB_OK or CB_EINVAL. */
+int cb_sched_set_batching(cb_sched* s, int batch_size, int max_wait);
+
+/* Real (not pad) tokens of the last cb_sched_step: all of them under
+ * continuous batching; under padded batching the prompt tokens of a padded
+ * prefill and, in a decode step, one per request still generating. */
+long long cb_sched_last_real_tokens(const cb_sched* s);
+
+/* Rolling KV cache ([KVB] "Rolling KV Cache"; reading: a query at position p
+ * sees keys p - window + 1 .. p, as in cb_paged_attention_window): at the end
+ * of every step each running request lets go of the blocks that its next
+ * query can no longer see (all positions before stored - window + 1); their
+ * block-table entries become -1, which the windowed attention calls never
+ * read.  A request publishes its shared prefix only while it holds all of it.
+ * window 0 (the default): no window.  Call before the first cb_sched_step.
+ * Returns CB_OK or CB_EINVAL (null handle, window < 0, or steps already run). */
+int cb_sched_set_window(cb_sched* s, int window);
+
 /* Register a request (ids are assigned 0, 1, 2, ... in call order; calls must
  * come in non-decreasing arrival_step order).  Returns the id or CB_EINVAL. */
 int cb_sched_add_request(cb_sched* s, int arrival_step, int prompt_len, int output_len);
@@ -335,7 +406,8 @@ int cb_sched_request_info(const cb_sched* s, int req_id, int* produced, int* sto
  * 连续内存分配: TraditionalKVCache) where the paged pool takes a block only when
  * the last one is full ([SM] PagedAttention 批处理).  out (host int64 [4]):
  *  out[0] running requests,
- *  out[1] tokens whose K/V the running requests have stored,
+ *  out[1] tokens whose K/V the running requests have stored and still hold
+ *         (a rolling window lets go of whole blocks),
  *  out[2] token slots in the blocks taken from the pool (held blocks x block_size),
  *  out[3] token slots a contiguous cache would reserve (out[0] x max_seq_len).
  * Paged waste = 1 - out[1] / out[2]; contiguous waste = 1 - out[1] / out[3].

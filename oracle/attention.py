@@ -20,6 +20,12 @@ What one continuous-batching attention step computes, written out plainly:
   does not say which query heads share a KV head): contiguous groups, query
   head h uses KV head h // (Hq / Hkv), as torch's ``enable_gqa`` does.
 
+* [KVB] §Rolling KV Cache (a heading with no body).  Reading: a rolling cache
+  keeps each request's W most recent keys, so a query at absolute position p
+  sees the keys at positions p - W + 1 .. p (its own included); W = 0 means no
+  window.  The cache's memory side (blocks that leave every window are freed)
+  belongs to the scheduler oracle.
+
 A row whose mask is all False has an undefined softmax; the oracle returns 0 for
 such a row (reading).  The causal step never produces one: every query sees its
 own key.
@@ -53,16 +59,19 @@ def masked_softmax_attention(Q, K, V, mask, scale):
     return O, P
 
 
-def chunk_causal_mask(q_len, n_cached):
+def chunk_causal_mask(q_len, n_cached, window=0):
     """Mask [q_len, n_cached + q_len] of a chunk after ``n_cached`` stored tokens.
 
     [CB] §Chunked prefill (stored KV prepended, mask adjusted) on top of the causal
     mask of [CB] §Attention: entry (i, j) is True iff j <= n_cached + i.  A decode
     step is the case q_len = 1 ([CB] §KV cache); a fresh prefill is n_cached = 0.
+    With a rolling window W > 0 ([KVB] §Rolling KV Cache, reading above) entry
+    (i, j) also needs j > n_cached + i - W.
     """
     mask = np.zeros((q_len, n_cached + q_len), dtype=bool)
     for i in range(q_len):
-        mask[i, : n_cached + i + 1] = True
+        lo = max(0, n_cached + i + 1 - window) if window > 0 else 0
+        mask[i, lo: n_cached + i + 1] = True
     return mask
 
 
@@ -91,7 +100,7 @@ def kv_head_of(h, n_q_heads, n_kv_heads):
     return h // (n_q_heads // n_kv_heads)
 
 
-def attention_step(q, q_lens, ctx_lens, k_seq, v_seq, scale, n_q_heads, n_kv_heads):
+def attention_step(q, q_lens, ctx_lens, k_seq, v_seq, scale, n_q_heads, n_kv_heads, window=0):
     """One attention step over a batch, request by request and head by head.
 
     q:        [nQ, Hq, A]   new query rows, requests concatenated in order.
@@ -99,6 +108,7 @@ def attention_step(q, q_lens, ctx_lens, k_seq, v_seq, scale, n_q_heads, n_kv_hea
     k_seq[r], v_seq[r]: [ctx_lens[r] + q_lens[r], Hkv, A] -- request r's stored
               keys/values followed by the new ones (the contiguous layout of
               [KVB] §连续内存分配).
+    window:   rolling-window length W (0: none), see ``chunk_causal_mask``.
     Returns out [nQ, Hq, A] in float64.
     """
     q = np.asarray(q, dtype=np.float64)
@@ -108,7 +118,7 @@ def attention_step(q, q_lens, ctx_lens, k_seq, v_seq, scale, n_q_heads, n_kv_hea
         K = np.asarray(k_seq[r], dtype=np.float64)
         V = np.asarray(v_seq[r], dtype=np.float64)
         assert K.shape[0] == cl + ql and V.shape[0] == cl + ql
-        mask = chunk_causal_mask(ql, cl)
+        mask = chunk_causal_mask(ql, cl, window)
         for h in range(n_q_heads):
             g = kv_head_of(h, n_q_heads, n_kv_heads)
             O, _ = masked_softmax_attention(q[t0:t0 + ql, h], K[:, g], V[:, g], mask, scale)
@@ -135,11 +145,12 @@ def attention_step_ragged(q, q_lens, ctx_lens, k_seq, v_seq, scale, n_q_heads, n
     return out
 
 
-def attention_rows(q_rows, k, v, positions, scale, n_q_heads, n_kv_heads):
+def attention_rows(q_rows, k, v, positions, scale, n_q_heads, n_kv_heads, window=0):
     """Selected query rows of one request (for sampled checks at large sizes).
 
     q_rows: [n, Hq, A] query rows at absolute positions ``positions`` (each row i
-    sees keys 0..positions[i]); k, v: [>= max(positions)+1, Hkv, A].
+    sees keys 0..positions[i], or with a rolling window W > 0 the keys
+    positions[i] - W + 1 .. positions[i]); k, v: [>= max(positions)+1, Hkv, A].
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -147,6 +158,8 @@ def attention_rows(q_rows, k, v, positions, scale, n_q_heads, n_kv_heads):
     out = np.zeros_like(q_rows)
     for i, p in enumerate(positions):
         mask = np.ones((1, p + 1), dtype=bool)
+        if window > 0:
+            mask[0, : max(0, p + 1 - window)] = False
         for h in range(n_q_heads):
             g = kv_head_of(h, n_q_heads, n_kv_heads)
             O, _ = masked_softmax_attention(q_rows[i:i + 1, h], k[:p + 1, g], v[:p + 1, g], mask, scale)

@@ -74,6 +74,13 @@ pages leave these points open):
    - a running request needing a block when none is free first drops the
      oldest published prefix (repeatedly) and only then preempts; admission
      neither drops prefixes nor preempts.
+8. Rolling window ([KVB] §Rolling KV Cache, a heading with no body; reading: a
+   query at position p sees keys p - W + 1 .. p).  With a window W > 0, at the
+   end of every step each running request lets go of the blocks that its next
+   query (at position ``stored``) can no longer see, i.e. whose positions all
+   lie before stored - W + 1; their table entries become -1 and they are never
+   read again.  A request publishes its prefix only while it still holds every
+   block of it.
 """
 from collections import deque
 from dataclasses import dataclass, field
@@ -118,10 +125,11 @@ def _blocks_for(n_tokens, block_size):
 
 
 class FCFSScheduler:
-    def __init__(self, requests, token_budget, block_size, num_blocks, free_order, max_batch=None):
+    def __init__(self, requests, token_budget, block_size, num_blocks, free_order, max_batch=None, window=0):
         """requests: iterable of (arrival_step, prompt_len, output_len[, group,
         prefix_len]), ids = index, sorted by arrival.  free_order: the initial
-        free-list order (a permutation of range(num_blocks))."""
+        free-list order (a permutation of range(num_blocks)).  window: rolling
+        window W (0: none; reading 8)."""
         self.reqs = []
         for i, t in enumerate(requests):
             a, p, o = (int(x) for x in t[:3])
@@ -133,6 +141,7 @@ class FCFSScheduler:
         assert sorted(int(b) for b in free_order) == list(range(num_blocks))
         self.budget = int(token_budget)
         self.max_batch = int(max_batch) if max_batch is not None else None
+        self.window = int(window)
         self.bs = int(block_size)
         self.num_blocks = int(num_blocks)
         self.free = deque(int(b) for b in free_order)
@@ -162,8 +171,19 @@ class FCFSScheduler:
 
     def _release(self, req):
         for b in req.blocks:
-            self._let_go(b)
+            if b >= 0:
+                self._let_go(b)
         req.blocks = []
+
+    def _slide(self, req):
+        """Rolling window: let go of the blocks the next query cannot see."""
+        if self.window <= 0:
+            return
+        first_seen = req.stored - self.window + 1
+        for i in range(min(len(req.blocks), max(0, first_seen) // self.bs)):
+            if req.blocks[i] >= 0:
+                self._let_go(req.blocks[i])
+                req.blocks[i] = -1
 
     def _drop_oldest_prefix(self):
         if not self.published:
@@ -178,6 +198,8 @@ class FCFSScheduler:
         if req.group < 0 or req.group in self.published or req.stored < req.prefix_len:
             return
         blocks = req.blocks[:_blocks_for(req.prefix_len, self.bs)]
+        if any(b < 0 for b in blocks):
+            return                                  # part of it already left the window
         for b in blocks:
             self.holders[b] += 1
         self.published[req.group] = (list(blocks), req.prefix_len, self.n_published)
@@ -200,7 +222,9 @@ class FCFSScheduler:
         ([KVB] 连续内存分配: the TraditionalKVCache reservation; [SM] PagedAttention
         批处理: a block is taken only when the last one is full)."""
         running = len(self.running)
-        stored = sum(r.stored for r in self.running)
+        # tokens whose K/V the running requests still hold (a rolling window
+        # lets go of whole blocks of stored tokens)
+        stored = sum(r.stored - self.bs * sum(1 for b in r.blocks if b < 0) for r in self.running)
         paged = (self.num_blocks - len(self.free)) * self.bs
         return dict(running=running, stored=stored, paged=paged, contiguous=running * int(max_seq_len))
 
@@ -335,6 +359,8 @@ class FCFSScheduler:
                 self._release(req)
                 self.running.remove(req)
                 meta.finished.append(req.rid)
+            else:
+                self._slide(req)
         self.now += 1
         return meta
 
@@ -343,3 +369,131 @@ class FCFSScheduler:
         while not self.done() and self.now < max_steps:
             out.append(self.step())
         return out
+
+
+class PaddedBatcher:
+    """Static and dynamic batching with padding, the baselines that continuous
+    batching is measured against.
+
+    Sources: [CB] §Continuous batching (batched generation: every prompt of the
+    batch is padded on the left to the batch's longest prompt, and the batch runs
+    until its longest generation ends); [SM] §动态批处理 (dynamic batching: the
+    requests that arrive within a waiting window, or until the batch is full, run
+    together as one batch) and §连续批处理 (continuous batching, for comparison).
+
+    Readings (the pages describe the policies, not their parameters):
+    1. A batch forms only when no batch is running, from the waiting requests in
+       arrival order, at most ``batch_size`` of them.  Static batching
+       (max_wait None) waits until batch_size requests are waiting or no further
+       request will arrive; dynamic batching also starts a batch once its oldest
+       waiting request has waited max_wait steps since its arrival.
+    2. The batch's first step is its padded prefill: every request processes
+       n_max positions (n_max = the longest prompt; the first n_max - P positions
+       are pads), all in one step, and produces its first token.  Then the batch
+       decodes one position per request per step until the longest output is
+       done: o_max - 1 decode steps; a request that has finished keeps decoding
+       pad positions.  So each request processes n_max + o_max - 1 positions.
+    3. Pad positions are computed and stored like real ones; the real tokens of
+       a request are its P prompt tokens and its O - 1 decoded positions.
+    4. Blocks are taken on demand from the FIFO free list (a block when the last
+       is full, as in FCFSScheduler) and all return when the batch ends.  A
+       request whose padded length cannot fit the pool is rejected on arrival;
+       a batch is cut short, from its end, until its padded length fits the
+       pool.
+    """
+
+    def __init__(self, requests, batch_size, block_size, num_blocks, free_order, max_wait=None):
+        self.reqs = [Request(i, int(a), int(p), int(o)) for i, (a, p, o) in enumerate(t[:3] for t in requests)]
+        arrivals = [r.arrival for r in self.reqs]
+        assert arrivals == sorted(arrivals), "requests must be given in arrival order"
+        assert sorted(int(b) for b in free_order) == list(range(num_blocks))
+        self.B = int(batch_size)
+        self.max_wait = None if max_wait is None else int(max_wait)
+        self.bs = int(block_size)
+        self.num_blocks = int(num_blocks)
+        self.free = deque(int(b) for b in free_order)
+        self.pending = deque(self.reqs)
+        self.waiting = []
+        self.batch = []            # running batch, arrival order
+        self.n_max = self.o_max = 0
+        self.k = 0                 # steps the batch has run
+        self.now = 0
+
+    def done(self):
+        return not self.pending and not self.waiting and not self.batch
+
+    def _blocks(self, n):
+        return -(-n // self.bs)
+
+    def _form_batch(self):
+        if self.batch or not self.waiting:
+            return
+        full = len(self.waiting) >= self.B
+        last = not self.pending
+        timed_out = self.max_wait is not None and self.now - self.waiting[0].arrival >= self.max_wait
+        if not (full or last or timed_out):
+            return
+        b = self.waiting[:self.B]
+        while b:
+            n_max = max(r.prompt_len for r in b)
+            o_max = max(r.output_len for r in b)
+            if len(b) * self._blocks(n_max + o_max - 1) <= self.num_blocks:
+                break
+            b = b[:-1]
+        self.batch = b
+        del self.waiting[:len(b)]
+        self.n_max = max(r.prompt_len for r in b)
+        self.o_max = max(r.output_len for r in b)
+        self.k = 0
+        for r in b:
+            r.state = "running"
+
+    def step(self):
+        """One step; returns (StepMetadata, real tokens of the step)."""
+        while self.pending and self.pending[0].arrival <= self.now:
+            r = self.pending.popleft()
+            if self._blocks(r.prompt_len + r.output_len - 1) > self.num_blocks:
+                r.state = "rejected"
+                continue
+            r.state = "waiting"
+            self.waiting.append(r)
+        self._form_batch()
+        sched = []
+        real = 0
+        if self.batch:
+            for r in self.batch:
+                if self.k == 0:
+                    n, c = self.n_max, 0
+                    real += r.prompt_len
+                else:
+                    n, c = 1, self.n_max + self.k - 1
+                    real += 1 if self.k < r.output_len else 0
+                need = self._blocks(c + n) - len(r.blocks)
+                for _ in range(need):
+                    r.blocks.append(self.free.popleft())
+                sched.append((r, n, c))
+        slots = []
+        for r, n, c in sched:
+            for p in range(c, c + n):
+                slots.append(r.blocks[p // self.bs] * self.bs + p % self.bs)
+        meta = StepMetadata(step=self.now, req_ids=np.array([r.rid for r, _, _ in sched], dtype=np.int32),
+                            q_lens=np.array([n for _, n, _ in sched], dtype=np.int32),
+                            ctx_lens=np.array([c for _, _, c in sched], dtype=np.int32),
+                            block_tables=[list(r.blocks) for r, _, _ in sched],
+                            slot_mapping=np.array(slots, dtype=np.int64), preempted=[], finished=[])
+        if self.batch:
+            for r, n, _ in sched:
+                r.stored += n
+                if self.k < r.output_len:
+                    r.produced = min(r.output_len, self.k + 1)
+            self.k += 1
+            if self.k == self.o_max:                     # the longest generation is done
+                for r in self.batch:
+                    for b in r.blocks:
+                        self.free.append(b)
+                    r.blocks = []
+                    r.state = "finished"
+                    meta.finished.append(r.rid)
+                self.batch = []
+        self.now += 1
+        return meta, real

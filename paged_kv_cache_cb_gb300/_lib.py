@@ -32,6 +32,12 @@ SIGNATURES = [
     ("cb_kv_append_paged_attention", _c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                               _c_int, _vp, _vp, _c_int, _vp, _c_float, _c_int, _c_int, _c_int,
                                               _c_int, _vp, _c_size, _vp]),
+    ("cb_paged_attention_window", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                           _c_int, _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                           _c_size, _vp]),
+    ("cb_kv_append_paged_attention_window", _c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                                     _c_int, _c_int, _vp, _vp, _c_int, _vp, _c_float, _c_int,
+                                                     _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     ("cb_paged_attention_noalloc", _c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
                                             _c_int, _vp, _c_float, _c_int, _c_int, _c_int, _c_int, _vp]),
     ("cb_last_error", _c_int, [_vp]),
@@ -41,6 +47,9 @@ SIGNATURES = [
     ("cb_build_slot_mapping", _c_int, [_i32p, _i32p, _i32p, _c_int, _c_int, _c_int, _i64p]),
     ("cb_sched_create", _vp, [_c_int, _c_int, _c_int, _c_int, _i32p]),
     ("cb_sched_destroy", None, [_vp]),
+    ("cb_sched_set_window", _c_int, [_vp, _c_int]),
+    ("cb_sched_set_batching", _c_int, [_vp, _c_int, _c_int]),
+    ("cb_sched_last_real_tokens", ctypes.c_longlong, [_vp]),
     ("cb_sched_add_request", _c_int, [_vp, _c_int, _c_int, _c_int]),
     ("cb_sched_add_request_prefix", _c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int]),
     ("cb_sched_step", _c_int, [_vp, _i32p, _i32p, _i32p, _i32p, _i32p, _c_int, _i64p, _intp, _intp]),
@@ -164,6 +173,20 @@ def cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, o
     """q, out: bf16 [n_tokens, Hq, A]; cu_q_lens int32 [n_reqs+1]; ctx_lens int32 [n_reqs];
     block_tables int32 [n_reqs, max_blocks]; caches bf16 [num_blocks, Hkv, bs, A];
     workspace: uint8 CUDA tensor of at least cb_paged_attention_workspace_size bytes."""
+    _attention("cb_paged_attention", None, q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, out, scale,
+               workspace, max_q_len, max_kv_len, stream)
+
+
+def cb_paged_attention_window(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, out, scale, workspace,
+                              max_q_len, max_kv_len, window, stream=None):
+    """cb_paged_attention with a rolling window: a query at position p sees the
+    keys p - window + 1 .. p (window 0: all)."""
+    _attention("cb_paged_attention_window", int(window), q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, out,
+               scale, workspace, max_q_len, max_kv_len, stream)
+
+
+def _attention(name, window, q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, out, scale, workspace,
+               max_q_len, max_kv_len, stream):
     torch = _t()
     bf = torch.bfloat16
     pq = _dev(q, bf, "q", 3)
@@ -181,10 +204,11 @@ def cb_paged_attention(q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache, o
     nb, hk, bs, a2 = k_cache.shape
     if v_cache.shape != k_cache.shape or a2 != a:
         raise ValueError("cache shape mismatch")
-    rc = lib().cb_paged_attention(pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok, int(max_q_len),
-                                  int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs, pw,
-                                  workspace.numel(), _stream(stream))
-    _check("cb_paged_attention", rc)
+    w = () if window is None else (window,)
+    rc = getattr(lib(), name)(pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok, int(max_q_len),
+                              int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs, *w, pw,
+                              workspace.numel(), _stream(stream))
+    _check(name, rc)
 
 
 def cb_kv_append_paged_attention(k_new, v_new, slot_mapping, q, cu_q_lens, ctx_lens, block_tables, k_cache, v_cache,
@@ -192,6 +216,20 @@ def cb_kv_append_paged_attention(k_new, v_new, slot_mapping, q, cu_q_lens, ctx_l
     """cb_kv_append of the step's new rows, then cb_paged_attention, as one call
     (one kernel launch where the attention launch is cooperative).  Arguments as
     for those two; k_new, v_new: bf16 [n_tokens, Hkv, A] with n_tokens = q's."""
+    _append_attention("cb_kv_append_paged_attention", None, k_new, v_new, slot_mapping, q, cu_q_lens, ctx_lens,
+                      block_tables, k_cache, v_cache, out, scale, workspace, max_q_len, max_kv_len, stream)
+
+
+def cb_kv_append_paged_attention_window(k_new, v_new, slot_mapping, q, cu_q_lens, ctx_lens, block_tables, k_cache,
+                                        v_cache, out, scale, workspace, max_q_len, max_kv_len, window, stream=None):
+    """cb_kv_append_paged_attention with a rolling window (see
+    cb_paged_attention_window)."""
+    _append_attention("cb_kv_append_paged_attention_window", int(window), k_new, v_new, slot_mapping, q, cu_q_lens,
+                      ctx_lens, block_tables, k_cache, v_cache, out, scale, workspace, max_q_len, max_kv_len, stream)
+
+
+def _append_attention(name, window, k_new, v_new, slot_mapping, q, cu_q_lens, ctx_lens, block_tables, k_cache,
+                      v_cache, out, scale, workspace, max_q_len, max_kv_len, stream):
     torch = _t()
     bf = torch.bfloat16
     pk = _dev(k_new, bf, "k_new", 3)
@@ -214,10 +252,11 @@ def cb_kv_append_paged_attention(k_new, v_new, slot_mapping, q, cu_q_lens, ctx_l
         raise ValueError("cache shape mismatch")
     if k_new.shape != (n_tok, hk, a) or v_new.shape != k_new.shape or slot_mapping.numel() != n_tok:
         raise ValueError("new rows must be [n_tokens, Hkv, A] with one slot per token")
-    rc = lib().cb_kv_append_paged_attention(pk, pv, ps, pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok,
-                                            int(max_q_len), int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk,
-                                            a, bs, pw, workspace.numel(), _stream(stream))
-    _check("cb_kv_append_paged_attention", rc)
+    w = () if window is None else (window,)
+    rc = getattr(lib(), name)(pk, pv, ps, pq, pcu, pctx, pbt, block_tables.shape[1], n_reqs, n_tok, int(max_q_len),
+                              int(max_kv_len), ck, cv, nb, po, float(scale), hq, hk, a, bs, *w, pw,
+                              workspace.numel(), _stream(stream))
+    _check(name, rc)
 
 
 CB_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -301,11 +340,16 @@ class Scheduler:
 
     STATES = ("pending", "waiting", "running", "finished", "rejected")
 
-    def __init__(self, num_blocks, block_size, token_budget, max_batch, free_order, max_blocks_per_seq):
+    def __init__(self, num_blocks, block_size, token_budget, max_batch, free_order, max_blocks_per_seq, window=0,
+                 padded_batch=0, max_wait=-1):
         fo, pfo = _i32(free_order)
         self._h = lib().cb_sched_create(num_blocks, block_size, token_budget, max_batch, pfo)
         if not self._h:
             raise CBError("cb_sched_create", CB_EINVAL)
+        if window:
+            _check("cb_sched_set_window", lib().cb_sched_set_window(self._h, int(window)))
+        if padded_batch:
+            _check("cb_sched_set_batching", lib().cb_sched_set_batching(self._h, int(padded_batch), int(max_wait)))
         self.max_batch = max_batch
         self.token_budget = token_budget
         self.max_blocks = max_blocks_per_seq
@@ -373,4 +417,5 @@ class Scheduler:
         b, t = nr.value, nt.value
         return dict(req_ids=self._req_ids[:b].copy(), q_lens=self._q[:b].copy(), ctx_lens=self._c[:b].copy(),
                     cu_q_lens=self._cu[:b + 1].copy(), block_tables=self._bt[:b].copy(),
-                    slot_mapping=self._sm[:t].copy(), n_preempted=rc)
+                    slot_mapping=self._sm[:t].copy(), n_preempted=rc,
+                    real_tokens=int(lib().cb_sched_last_real_tokens(self._h)))

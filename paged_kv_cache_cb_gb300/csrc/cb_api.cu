@@ -181,8 +181,12 @@ WorkspaceLayout layout_for_splits(long long splits, int n_reqs, int n_q_heads, i
   return L;
 }
 
+// Shapes of the block-tile decode (128-row tiles of whole blocks): head_dim 128
+// with 8 KV heads and G >= 2, or 32 query heads on 2 KV heads (G = 16) or on 1
+// (MQA, G = 32).
 bool block_tile_shape(int n_q_heads, int n_kv_heads, int head_dim) {
-  return head_dim == 128 && n_kv_heads == 8 && n_q_heads / n_kv_heads >= 2;
+  if (head_dim != 128 || n_q_heads % n_kv_heads) return false;
+  return (n_kv_heads == 8 && n_q_heads / n_kv_heads >= 2) || (n_q_heads == 32 && (n_kv_heads == 2 || n_kv_heads == 1));
 }
 
 }  // namespace
@@ -228,10 +232,11 @@ namespace {
 
 bool shape_ok(int n_q_heads, int n_kv_heads, int head_dim, int block_size) {
   if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return false;
-  const int g = n_q_heads / n_kv_heads;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return false;
   if (head_dim != 64 && head_dim != 128) return false;
-  return block_size == kBlockSize;
+  if (block_size != kBlockSize) return false;
+  const int g = n_q_heads / n_kv_heads;
+  if (g == 1 || g == 2 || g == 4 || g == 8) return true;
+  return block_tile_shape(n_q_heads, n_kv_heads, head_dim);    // G = 16, 32
 }
 
 }  // namespace
@@ -319,9 +324,9 @@ struct AppendArgs {
 int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
                    const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens, int max_q_len,
                    int max_kv_len, const void* k_cache, const void* v_cache, int num_blocks, void* out, float scale,
-                   int n_q_heads, int n_kv_heads, int head_dim, int block_size, void* workspace,
+                   int n_q_heads, int n_kv_heads, int head_dim, int block_size, int window, void* workspace,
                    size_t workspace_bytes, void* stream) {
-  if (!shape_ok(n_q_heads, n_kv_heads, head_dim, block_size)) return CB_EINVAL;
+  if (!shape_ok(n_q_heads, n_kv_heads, head_dim, block_size) || window < 0) return CB_EINVAL;
   if (n_reqs < 0 || n_reqs > CB_MAX_REQS || n_tokens < 0 || max_q_len < 1 || max_kv_len < 1 ||
       max_blocks_per_seq < 1 || num_blocks <= 0 || !(scale > 0.f) || max_q_len > max_kv_len)
     return CB_EINVAL;
@@ -364,6 +369,7 @@ int attention_step(const AppendArgs* app, const void* q, const int32_t* cu_q_len
   p.n_q_heads = n_q_heads;
   p.n_kv_heads = n_kv_heads;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = window;
   p.split_blocks = choose_split_blocks(n_reqs, max_kv_len, n_kv_heads, di.n_sms);
   p.max_splits_total = L.max_splits_total;
   p.counters = reinterpret_cast<int*>(ws + L.counters);
@@ -445,7 +451,17 @@ int cb_paged_attention(const void* q, const int32_t* cu_q_lens, const int32_t* c
                        size_t workspace_bytes, void* stream) {
   return attention_step(nullptr, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens,
                         max_q_len, max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads,
-                        head_dim, block_size, workspace, workspace_bytes, stream);
+                        head_dim, block_size, 0, workspace, workspace_bytes, stream);
+}
+
+int cb_paged_attention_window(const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                              const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                              int max_q_len, int max_kv_len, const void* k_cache, const void* v_cache, int num_blocks,
+                              void* out, float scale, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                              int window, void* workspace, size_t workspace_bytes, void* stream) {
+  return attention_step(nullptr, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens,
+                        max_q_len, max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads,
+                        head_dim, block_size, window, workspace, workspace_bytes, stream);
 }
 
 int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
@@ -457,7 +473,20 @@ int cb_kv_append_paged_attention(const void* k_new, const void* v_new, const int
   const AppendArgs app{k_new, v_new, slot_mapping};
   return attention_step(&app, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens, max_q_len,
                         max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads, head_dim,
-                        block_size, workspace, workspace_bytes, stream);
+                        block_size, 0, workspace, workspace_bytes, stream);
+}
+
+int cb_kv_append_paged_attention_window(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                        const void* q, const int32_t* cu_q_lens, const int32_t* ctx_lens,
+                                        const int32_t* block_tables, int max_blocks_per_seq, int n_reqs, int n_tokens,
+                                        int max_q_len, int max_kv_len, void* k_cache, void* v_cache, int num_blocks,
+                                        void* out, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int block_size, int window, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  const AppendArgs app{k_new, v_new, slot_mapping};
+  return attention_step(&app, q, cu_q_lens, ctx_lens, block_tables, max_blocks_per_seq, n_reqs, n_tokens, max_q_len,
+                        max_kv_len, k_cache, v_cache, num_blocks, out, scale, n_q_heads, n_kv_heads, head_dim,
+                        block_size, window, workspace, workspace_bytes, stream);
 }
 
 int cb_last_error(void* stream) {

@@ -31,6 +31,12 @@ namespace cb {
 #define kNegInf (-__int_as_float(0x7f800000))
 
 // ---------------------------------------------------------------- planning
+// First block a decode with kv keys reads under a rolling window W: the block
+// holding position kv - W, its first visible key (0 without a window).
+__device__ __forceinline__ int window_first_block(long long kv, int window) {
+  return window > 0 && kv > window ? (int)((kv - window) / kBlockSize) : 0;
+}
+
 // Work counts of request r.  Validates the metadata; a bad request gets no work
 // and sets CB_DEVERR_BADLEN.
 struct ReqWork {
@@ -50,7 +56,8 @@ __device__ __forceinline__ ReqWork request_work(const StepParams& P, int r, int 
     return w;
   }
   if (q_len == 1) {
-    w.splits = (int)((nblk + P.split_blocks - 1) / P.split_blocks);
+    const long long nb = nblk - window_first_block(kv, P.window);   // the blocks the window reaches
+    w.splits = (int)((nb + P.split_blocks - 1) / P.split_blocks);
     w.dec_items = w.splits * P.n_kv_heads;
   } else if (q_len > 1) {
     if (!allow_prefill) {
@@ -168,8 +175,9 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
   const int t = __ldg(P.cu_q_lens + r);            // the request's single new token
   const int kv = __ldg(P.ctx_lens + r) + 1;
   const int nblk = (kv + kBlockSize - 1) / kBlockSize;
-  const int b0 = split * P.split_blocks;
+  const int b0 = window_first_block(kv, P.window) + split * P.split_blocks;
   const int nb = min(P.split_blocks, nblk - b0);
+  const int key_lo = P.window > 0 ? kv - P.window : 0;     // first visible key (rolling window)
 
   // query rows of the group -> shared fp32, pre-scaled
   {
@@ -266,7 +274,7 @@ __device__ bool decode_item(const StepParams& P, const CUtensorMap* kmap, const 
         s[j] = (a + b) + (c + d);
       }
     }
-    const bool tvalid = tokbase + tq < kv;
+    const bool tvalid = tokbase + tq < kv && tokbase + tq >= key_lo;
 #pragma unroll
     for (int j = 0; j < G; ++j) {
       s[j] += __shfl_xor_sync(FULL, s[j], 16);

@@ -1,18 +1,24 @@
-// The block-tile GQA decode pipeline (8 KV heads, head_dim 128), shared by the
-// decode kernel (cb_decode_tcb.cu) and the decode phase of the mixed kernel
-// (cb_mixed.cu).
+// The block-tile decode pipeline (head_dim 128; 8 KV heads, or MQA / GQA with
+// 1 or 2 KV heads and 32 query heads), shared by the decode kernel
+// (cb_decode_tcb.cu) and the decode phase of the mixed kernel (cb_mixed.cu).
 //
 // [CB] KV cache: each request's new token attends over all its stored keys;
 // [KVN] MQA/GQA: query head h reads KV head h / G.  In the cache layout
-// [block][KV head][16 tokens][128], one block of all 8 KV heads is 128
-// contiguous rows, so a K (or V) tile is two 128-row x 64-column TMA boxes of
-// 16 KB -- an eighth of the TMA operations that per-head 16-row boxes need, and
-// exactly an M = 128 MMA operand.  Row i of a tile is (KV head i/16, token i%16).
+// [block][KV head][16 tokens][128], one block of all HKV KV heads is 16 * HKV
+// contiguous rows, so a 128-row tile is BPT = 8 / HKV consecutive blocks of the
+// request's table: one block of 8 heads, or 8 blocks of the single MQA head.
+// Each block is fetched as two 16*HKV-row x 64-column TMA boxes; a tile is
+// exactly an M = 128 MMA operand.  Row i of a tile is (block i / (16 HKV) of
+// the tile, KV head (i / 16) % HKV, token i % 16).
 //     S[rows, q heads]   = K_tile . q^T                 (M=128, N=Hq, K=128 dims)
 //     O^T[dims, q heads] += V_tile^T . P^T              (M=128, N=Hq, K=128 rows)
 // P[h, row] is non-zero only where row's KV head is h/G (the GQA head mapping
-// written as a block-diagonal matrix): the off-diagonal zeros are written once
-// and the softmax threads rewrite only the diagonal entries.
+// written as a block-structured matrix): the zeros are written once and the
+// softmax threads rewrite only the entries of their rows' heads.  With 8 KV
+// heads each head's rows of a tile are the 16 rows of one half-warp; with 1 or
+// 2 KV heads a head's rows span all four softmax warps, so its tile maximum
+// and its row sums are reduced across the warps (a transpose-reduce inside each
+// warp leaves lane l with q head l, then shared memory).
 //
 // Work: the decode requests' blocks, laid end to end in request order and cut
 // into equal chunks of W blocks (W in [4, 32], chosen to fill the grid in the
@@ -53,47 +59,55 @@ namespace tcb {
 
 constexpr int kThreads = 352;
 constexpr int kMergeTid0 = 224;   // epilogue warps 7-10
-constexpr int kHkv = 8;
 constexpr int kChunksPerCta = 4;   // most rounds of chunks per CTA
 constexpr int kRoundBlocks = 8;    // blocks per CTA per round before a step takes another round
 constexpr int kMinChunk = 4;       // blocks
 
-template <int G>
+// Shapes: HKV KV heads (8, 2 or 1), G query heads per KV head; Hq = HKV * G.
+template <int G, int HKV = 8>
 struct Cfg {
-  static constexpr int Hq = 8 * G;
-  static constexpr int KS = G == 8 ? 2 : 3;          // K ring stages
+  static_assert(HKV == 8 || HKV == 2 || HKV == 1, "KV heads");
+  static_assert(HKV == 8 || HKV * G == 32, "with fewer than 8 KV heads: 32 query heads");
+  static constexpr int Hq = HKV * G;
+  static constexpr int BPT = 8 / HKV;                 // physical blocks per 128-row tile
+  static constexpr int KS = Hq == 64 ? 2 : 3;         // K ring stages
   static constexpr int VS = 2;                        // V ring stages
   static constexpr int TM = Hq <= 16 ? 128 : Hq <= 32 ? 256 : 512;   // TMEM columns: S x3, O x2, Hq each
+  static constexpr int MaxW = 32 * BPT;               // most blocks in a chunk (32 tiles' worth of table entries / lanes)
 };
 
-template <int G>
+template <int G, int HKV = 8>
 struct Tiles {
-  static constexpr int Hq = Cfg<G>::Hq;
-  uint8_t k[Cfg<G>::KS][2][128][128];   // [stage][dim half][row][128 B]
-  uint8_t v[Cfg<G>::VS][2][128][128];
+  static constexpr int Hq = Cfg<G, HKV>::Hq;
+  uint8_t k[Cfg<G, HKV>::KS][2][128][128];   // [stage][dim half][row][128 B]
+  uint8_t v[Cfg<G, HKV>::VS][2][128][128];
   uint8_t q[2][2][Hq][128];            // [buffer][dim half][q head][128 B]
   uint8_t p[2][2][Hq][128];            // [buffer][row half][q head][128 B]: K-major B of O^T += V^T P^T
 };
 
 // One segment: request r (query token t, kv keys), split `split` of nsplit
-// (partials at slot0 + split), blocks [b0, b0 + nb) of its table.
+// (partials at slot0 + split), blocks [b0, b0 + nb) of its table, in nt tiles
+// of BPT blocks (the last one possibly partial).
 struct BItem {
-  int r, split, nsplit, slot0, t, kv, b0, nb;
+  int r, split, nsplit, slot0, t, kv, b0, nb, nt;
 };
 
-template <int G>
-struct Ctl {
-  static constexpr int Hq = Cfg<G>::Hq;
+// 16-byte aligned (its size too), so that xr's float4 reads are aligned
+// wherever a kernel places it after another 16-byte aligned region.
+template <int G, int HKV = 8>
+struct alignas(16) Ctl {
+  static constexpr int Hq = Cfg<G, HKV>::Hq;
   uint64_t item_full[2], item_empty[2], q_full[2], q_empty[2];
-  uint64_t k_full[Cfg<G>::KS], k_empty[Cfg<G>::KS], v_full[Cfg<G>::VS], v_empty[Cfg<G>::VS];
+  uint64_t k_full[Cfg<G, HKV>::KS], k_empty[Cfg<G, HKV>::KS], v_full[Cfg<G, HKV>::VS], v_empty[Cfg<G, HKV>::VS];
   uint64_t s_full[3], p_full[2], p_empty[2], o_done[2], drain;
   BItem item[2];               // the segment published in each slot (r < 0: no more work)
-  int rows[2][kMaxSplitBlocks];   // its blocks' first cache rows
+  int rows[2][Cfg<G, HKV>::MaxW];   // its blocks' first cache rows
   struct {
     int cu, ctx, pad[2];
-    int bt[kMaxSplitBlocks];
+    int bt[Cfg<G, HKV>::MaxW];
   } raw[2];                    // an item's metadata as copied from global memory
   float alpha[2][Hq];          // per-tile rescale factors of O, per q head
+  alignas(16) float xr[4][32];   // fewer than 8 KV heads: per-warp maxima / sums, lane = q head (float4 reads)
   struct {
     BItem I;                   // r < 0: no more segments
     uint32_t last_pv;
@@ -141,7 +155,7 @@ __device__ __forceinline__ int decode_blocks(const StepParams& P, int r, bool al
     set_error(P.err, CB_DEVERR_BADLEN);
     return 0;
   }
-  return (int)nblk;
+  return (int)nblk - window_first_block(kv, P.window);   // the blocks its rolling window reaches
 }
 
 // Exclusive prefix sum of a[0..n) in place, a[n] = total (returned).  All
@@ -189,16 +203,20 @@ __device__ inline int block_scan_excl(int* a, int n, int* scratch) {
 // W = ceil(total / (R * grid)) in [kMinChunk, 32], raised if the partial
 // buffers could not hold the splits (n + chunks).  All threads call it; every
 // CTA computes the same plan.  Ends with __syncthreads().
-template <int G>
-__device__ void finish_plan(const StepParams& P, Ctl<G>& C, int* bpre, int* slot) {
+template <int G, int HKV>
+__device__ void finish_plan(const StepParams& P, Ctl<G, HKV>& C, int* bpre, int* slot) {
   const int n = P.n_reqs, tid = threadIdx.x, T = blockDim.x;
   const int total = block_scan_excl(bpre, n, C.scratch);
+  constexpr int BPT = Cfg<G, HKV>::BPT;
   const long long grid = gridDim.x;
-  const long long R = max(1LL, min((long long)kChunksPerCta, (total + kRoundBlocks * grid - 1) / (kRoundBlocks * grid)));
+  // a round is kRoundBlocks 8-head blocks' worth of K/V per CTA: BPT blocks of fewer heads each
+  const long long rb = (long long)kRoundBlocks * BPT;
+  const long long R = max(1LL, min((long long)kChunksPerCta, (total + rb * grid - 1) / (rb * grid)));
   long long want = (total + R * grid - 1) / (R * grid);
   const long long cap = max(1LL, (long long)P.max_splits_total - n);   // chunks the partial buffers can take
   want = max(want, (total + cap - 1) / cap);
-  const int W = (int)max((long long)kMinChunk, min((long long)kMaxSplitBlocks, want));
+  want = (want + BPT - 1) / BPT * BPT;           // whole tiles
+  const int W = (int)max((long long)kMinChunk, min((long long)Cfg<G, HKV>::MaxW, want));
   for (int i = tid; i < n; i += T) {
     const int blk = bpre[i + 1] - bpre[i];
     slot[i] = blk > 0 ? (bpre[i] + blk - 1) / W - bpre[i] / W + 1 : 0;
@@ -220,8 +238,8 @@ __device__ void finish_plan(const StepParams& P, Ctl<G>& C, int* bpre, int* slot
 
 // Barrier set-up (one thread) and P's off-diagonal zeros (all threads; the
 // caller fences and synchronises before the pipeline starts).
-template <int G>
-__device__ void init_ctl(Ctl<G>& C) {
+template <int G, int HKV>
+__device__ void init_ctl(Ctl<G, HKV>& C) {
   for (int s = 0; s < 2; ++s) {
     mbar_init(&C.item_full[s], 1);
     mbar_init(&C.item_empty[s], 1 + 128 + 1);   // MMA, softmax threads, V producer
@@ -235,11 +253,11 @@ __device__ void init_ctl(Ctl<G>& C) {
     mbar_init(&C.o_full[s], 1);
     mbar_init(&C.o_free[s], 128);
   }
-  for (int s = 0; s < Cfg<G>::KS; ++s) {
+  for (int s = 0; s < Cfg<G, HKV>::KS; ++s) {
     mbar_init(&C.k_full[s], 1);
     mbar_init(&C.k_empty[s], 1);
   }
-  for (int s = 0; s < Cfg<G>::VS; ++s) {
+  for (int s = 0; s < Cfg<G, HKV>::VS; ++s) {
     mbar_init(&C.v_full[s], 1);
     mbar_init(&C.v_empty[s], 1);
   }
@@ -248,10 +266,20 @@ __device__ void init_ctl(Ctl<G>& C) {
   C.abort = 0;
   C.split_any = 0;
 }
-template <int G>
-__device__ void zero_p(Tiles<G>& T) {
+template <int G, int HKV>
+__device__ void zero_p(Tiles<G, HKV>& T) {
   for (int i = threadIdx.x; i < (int)sizeof(T.p) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(&T.p[0][0][0][0])[i] = make_uint4(0, 0, 0, 0);
+}
+
+// v[k] for a k that is the same in every lane (a select chain: an indexed
+// register array would live in local memory).
+template <int N>
+__device__ __forceinline__ int pick(const int (&v)[N], int k) {
+  int r = v[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) r = k == i ? v[i] : r;
+  return r;
 }
 
 // ---------------------------------------------------------------- K producer (warp 4)
@@ -260,15 +288,15 @@ __device__ void zero_p(Tiles<G>& T) {
 // tile or two before the current segment's last tile is issued, and the next
 // chunk is claimed (an atomic) a few tiles before that, so neither round trip
 // stalls the stream; claiming no earlier keeps the dynamic balance.
-template <int G>
-__device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* qmap, Tiles<G>& T,
-                           Ctl<G>& C, const int* bpre, const int* slot, bool static_first) {
-  constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS;
+template <int G, int HKV>
+__device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* qmap, Tiles<G, HKV>& T,
+                           Ctl<G, HKV>& C, const int* bpre, const int* slot, bool static_first) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, KS = Cfg<G, HKV>::KS, BPT = Cfg<G, HKV>::BPT;
   constexpr uint32_t kTileBytes = 2 * 128 * 128;
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int n = P.n_reqs, W = C.W, NC = C.NC, total = C.total;
-  const int rows_total = P.num_blocks * kHkv * kBlockSize;
+  const int rows_total = P.num_blocks * HKV * kBlockSize;
   auto find_pos = [&](int x) {     // the request whose blocks hold linear block x
     int lo = 0, hi = n - 1;
     while (lo < hi) {
@@ -281,13 +309,15 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     return lo;
   };
   auto fetch = [&](int i, int x, int buf) {
-    const int r = i, b0 = x - bpre[i];
+    const int r = i;
+    int b0 = x - bpre[i];          // the request's blocks start at its window's first block
+    if (P.window > 0) b0 += window_first_block((long long)__ldg(P.ctx_lens + r) + 1, P.window);
     if (lane == 0) {
       cp_async4(&C.raw[buf].cu, P.cu_q_lens + r);
       cp_async4(&C.raw[buf].ctx, P.ctx_lens + r);
     }
-    if (lane < W && b0 + lane < P.max_blocks_per_seq)
-      cp_async4(&C.raw[buf].bt[lane], P.block_tables + (size_t)r * P.max_blocks_per_seq + b0 + lane);
+    for (int b = lane; b < W && b0 + b < P.max_blocks_per_seq; b += 32)
+      cp_async4(&C.raw[buf].bt[b], P.block_tables + (size_t)r * P.max_blocks_per_seq + b0 + b);
     cp_async_commit();
   };
   // With static_first, CTA b starts on chunk b and the counter hands out the
@@ -313,26 +343,34 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     const int sl = it & 1;
     BItem I;
     I.r = -1;
-    int y = rows_total;            // this segment's physical blocks as cache rows, one per lane
+    // this segment's physical blocks as cache rows: block lane + 32 k in yv[k]
+    // (past the segment or the cache: beyond the extent, which TMA fills with zeros)
+    int yv[BPT];
+#pragma unroll
+    for (int k = 0; k < BPT; ++k) yv[k] = rows_total;
     int seg_end = 0;
     if (c >= 0) {
       cp_async_wait_all();
       __syncwarp();
       seg_end = min(end, bpre[i + 1]);
       I.r = i;
-      I.b0 = x - bpre[i];
+      I.b0 = x - bpre[i] + window_first_block((long long)C.raw[sl].ctx + 1, P.window);
       I.nb = seg_end - x;
+      I.nt = (I.nb + BPT - 1) / BPT;
       I.split = c - bpre[i] / W;
       I.nsplit = slot[i + 1] - slot[i];
       I.slot0 = slot[i];
       I.t = C.raw[sl].cu;
       I.kv = C.raw[sl].ctx + 1;
-      if (lane < I.nb) {
-        const int e = C.raw[sl].bt[lane];
-        if (e >= 0 && e < P.num_blocks)
-          y = e * kHkv * kBlockSize;
-        else
-          set_error(P.err, CB_DEVERR_BADBLOCK);   // rows past the cache read as zeros
+#pragma unroll
+      for (int k = 0; k < BPT; ++k) {
+        if (lane + 32 * k < I.nb) {
+          const int e = C.raw[sl].bt[lane + 32 * k];
+          if (e >= 0 && e < P.num_blocks)
+            yv[k] = e * HKV * kBlockSize;
+          else
+            set_error(P.err, CB_DEVERR_BADBLOCK);   // rows past the cache read as zeros
+        }
       }
       __syncwarp();                // raw[sl] is refilled two segments from now
     }
@@ -341,7 +379,10 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
       good = lwait(P, C, &C.item_empty[sl], ((it >> 1) & 1) ^ 1);
     }
     good = __shfl_sync(FULL, good, 0);
-    if (good) C.rows[sl][lane] = y;
+    if (good) {
+#pragma unroll
+      for (int k = 0; k < BPT; ++k) C.rows[sl][lane + 32 * k] = yv[k];
+    }
     __syncwarp();
     if (lane == 0) {
       if (good) {
@@ -363,10 +404,10 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
     if (I.r < 0) break;
     // the next segment: the rest of this chunk, else the first of a new chunk
     const bool chunk_done = seg_end >= end;
-    const int claim_at = chunk_done ? max(0, I.nb - 4) : -1, fetch_at = max(0, I.nb - 2);
+    const int claim_at = chunk_done ? max(0, I.nt - 4) : -1, fetch_at = max(0, I.nt - 2);
     // (requests with no decode token have no blocks and are skipped)
     int nc = c, nx = seg_end, ni = seg_end < end ? find_pos(seg_end) : i, nend = end, nraw = 0;
-    for (int j = 0; j < I.nb && ok; ++j) {
+    for (int j = 0; j < I.nt && ok; ++j) {
       if (j == claim_at) nraw = claim();
       if (j == fetch_at) {
         if (chunk_done) {
@@ -380,18 +421,19 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
         }
         if (nc >= 0) fetch(ni, nx, sl ^ 1);
       }
-      const int yb = __shfl_sync(FULL, y, j);
+      // tile j: blocks j*BPT .. j*BPT + BPT - 1 of the segment; lane L < 2 BPT
+      // loads half L % 2 of block L / 2 (all in one 32-block group of yv)
+      const int blk = j * BPT + ((lane >> 1) & (BPT - 1));
+      const int yb = __shfl_sync(FULL, pick<BPT>(yv, (j * BPT) >> 5), blk & 31);
+      const int ks = kt % KS;
       if (lane == 0) {
-        const int ks = kt % KS;
         good = lwait(P, C, &C.k_empty[ks], ((kt / KS) & 1) ^ 1);
-        if (good) {
-          mbar_arrive_expect_tx(&C.k_full[ks], kTileBytes);
-          tma_load_2d(&T.k[ks][0][0][0], kmap, 0, yb, &C.k_full[ks]);
-          tma_load_2d(&T.k[ks][1][0][0], kmap, 64, yb, &C.k_full[ks]);
-          ++kt;
-        }
+        if (good) mbar_arrive_expect_tx(&C.k_full[ks], kTileBytes);
       }
       ok = __shfl_sync(FULL, good, 0);
+      if (ok && lane < 2 * BPT)
+        tma_load_2d(&T.k[ks][lane & 1][(lane >> 1) * 16 * HKV][0], kmap, (lane & 1) * 64, yb, &C.k_full[ks]);
+      if (ok) ++kt;
     }
     c = nc;
     x = nx;
@@ -410,9 +452,9 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
 }
 
 // ---------------------------------------------------------------- V producer (warp 6)
-template <int G>
-__device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G>& T, Ctl<G>& C) {
-  constexpr int VS = Cfg<G>::VS;
+template <int G, int HKV>
+__device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G, HKV>& T, Ctl<G, HKV>& C) {
+  constexpr int VS = Cfg<G, HKV>::VS, BPT = Cfg<G, HKV>::BPT;
   constexpr uint32_t kTileBytes = 2 * 128 * 128;
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
@@ -426,24 +468,25 @@ __device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G
       ok = false;
       break;
     }
-    const int r = C.item[sl].r, nb = C.item[sl].nb;
-    const int y = C.rows[sl][lane];
+    const int r = C.item[sl].r, nt = C.item[sl].nt;
+    int yv[BPT];
+#pragma unroll
+    for (int k = 0; k < BPT; ++k) yv[k] = C.rows[sl][lane + 32 * k];
     __syncwarp();
     if (lane == 0) mbar_arrive(&C.item_empty[sl]);
     if (r < 0) break;
-    for (int j = 0; j < nb && ok; ++j) {
-      const int yb = __shfl_sync(FULL, y, j);
+    for (int j = 0; j < nt && ok; ++j) {
+      const int blk = j * BPT + ((lane >> 1) & (BPT - 1));
+      const int yb = __shfl_sync(FULL, pick<BPT>(yv, (j * BPT) >> 5), blk & 31);
+      const int vs = vt % VS;
       if (lane == 0) {
-        const int vs = vt % VS;
         good = lwait(P, C, &C.v_empty[vs], ((vt / VS) & 1) ^ 1);
-        if (good) {
-          mbar_arrive_expect_tx(&C.v_full[vs], kTileBytes);
-          tma_load_2d(&T.v[vs][0][0][0], vmap, 0, yb, &C.v_full[vs]);
-          tma_load_2d(&T.v[vs][1][0][0], vmap, 64, yb, &C.v_full[vs]);
-          ++vt;
-        }
+        if (good) mbar_arrive_expect_tx(&C.v_full[vs], kTileBytes);
       }
       ok = __shfl_sync(FULL, good, 0);
+      if (ok && lane < 2 * BPT)
+        tma_load_2d(&T.v[vs][lane & 1][(lane >> 1) * 16 * HKV][0], vmap, (lane & 1) * 64, yb, &C.v_full[vs]);
+      if (ok) ++vt;
     }
     ++it;
   }
@@ -457,9 +500,9 @@ __device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G
 // the three TMEM score buffers is free (S runs at most two tiles ahead of PV);
 // O += P(n) V(n) as soon as P(n) and V(n) are ready.  A late V tile then holds
 // up only its own PV, not the K stream behind it.
-template <int G>
-__device__ void b_mma(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
-  constexpr int Hq = Cfg<G>::Hq, KS = Cfg<G>::KS, VS = Cfg<G>::VS;
+template <int G, int HKV>
+__device__ void b_mma(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, KS = Cfg<G, HKV>::KS, VS = Cfg<G, HKV>::VS;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, Hq, 0, 0);
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, Hq, 0, 1);   // A = V^T: MN-major
   constexpr uint32_t kStage = (2 * 128 * 128) >> 4;              // one K/V stage, descriptor units
@@ -479,7 +522,7 @@ __device__ void b_mma(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem
   for (;;) {
     bool progress = false;
     if (!s_done && s_nb < 0 && mbar_ready(&C.item_full[s_it & 1], (s_it >> 1) & 1)) {
-      const int r = C.item[s_it & 1].r, nb = C.item[s_it & 1].nb;
+      const int r = C.item[s_it & 1].r, nb = C.item[s_it & 1].nt;   // tiles
       mbar_arrive(&C.item_empty[s_it & 1]);
       if (r < 0) {
         s_done = true;
@@ -584,13 +627,35 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
   }
 }
 
+// Transpose-reduce over groups of N consecutive lanes (N = 16 or 32), each
+// holding N values: afterwards v[0] of lane l is the maximum (MAX) or the sum
+// of value l % N over the group's lanes.  At the step with offset o a lane
+// keeps the half of its live values selected by bit o of its lane index and
+// swaps the other half with lane ^ o: N - 1 shuffles in all.
+template <int N, bool MAX>
+__device__ __forceinline__ void xreduce(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = N / 2; o >= 1; o >>= 1) {
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float keep = up ? v[i + o] : v[i];
+      const float send = up ? v[i] : v[i + o];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- softmax (warps 0-3)
-template <int G>
-__device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t tmem) {
-  constexpr int Hq = Cfg<G>::Hq, VS = Cfg<G>::VS;
-  const int tid = threadIdx.x;                 // tile row (KV head tid/16, token tid%16); output dimension
+template <int G, int HKV>
+__device__ void b_softmax(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, VS = Cfg<G, HKV>::VS, BPT = Cfg<G, HKV>::BPT;
+  const int tid = threadIdx.x;                 // tile row; output dimension
   const int warp = tid >> 5, lane = tid & 31;
-  const int g = tid >> 4, tok = tid & 15;
+  // tile row = (block bi of the tile, KV head g, token tok)
+  const int bi = tid / (16 * HKV), g = (tid >> 4) % HKV, tok = tid & 15;
   const bool hi = (lane >> 4) & 1;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   const float sl2 = P.scale_log2;
@@ -613,40 +678,85 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
       lp[i] = 0.f;
     }
     bool stop = false;
-    for (int j = 0; j < I.nb; ++j, ++sc) {
+    for (int j = 0; j < I.nt; ++j, ++sc) {
       const int sb = sc & 1;
-      const bool valid = (I.b0 + j) * kBlockSize + tok < I.kv;
+      const int bseg = j * BPT + bi;             // this row's block within the segment
+      const int pos = (I.b0 + bseg) * kBlockSize + tok;
+      const bool valid = bseg < I.nb && pos < I.kv && (P.window <= 0 || pos >= I.kv - P.window);
       bool need_any = false;
       const int sbuf = sc % 3;    // TMEM score buffer (sb: P buffer)
       good = wwait(P, C, &C.s_full[sbuf], (sc / 3) & 1);
+      float x[G];                 // scores of this row's G query heads, times scale * log2 e
       if (good) {
         tc_fence_after();
-        // this warp's two KV heads own columns [2*warp*G, 2*warp*G + 2G); each half-warp keeps its G
-        float sv[2 * G];
-        if constexpr (G == 2) {
-          float t8[8];
-          tmem_ld8(tmem + lane_base + sbuf * Hq + ((4 * warp) & ~7), t8);
-          tmem_wait_ld();
-          const bool upper = warp & 1;   // columns 4..7 of the 8 loaded
+        if constexpr (HKV == 8) {
+          // this warp's two KV heads own columns [2*warp*G, 2*warp*G + 2G); each half-warp keeps its G
+          float sv[2 * G];
+          if constexpr (G == 2) {
+            float t8[8];
+            tmem_ld8(tmem + lane_base + sbuf * Hq + ((4 * warp) & ~7), t8);
+            tmem_wait_ld();
+            const bool upper = warp & 1;   // columns 4..7 of the 8 loaded
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sv[i] = upper ? t8[4 + i] : t8[i];
+            for (int i = 0; i < 4; ++i) sv[i] = upper ? t8[4 + i] : t8[i];
+          } else {
+            tmem_ld_n<2 * G>(tmem + lane_base + sbuf * Hq + 2 * warp * G, sv);
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int i = 0; i < G; ++i) x[i] = valid ? (hi ? sv[G + i] : sv[i]) * sl2 : kNegInf;
         } else {
-          tmem_ld_n<2 * G>(tmem + lane_base + sbuf * Hq + 2 * warp * G, sv);
+          // Hq = 32 columns: the half-warps' KV heads (2 heads: columns [16 hw, 16 hw + 16); 1 head: all)
+          float sv[32];
+          tmem_ld_n<32>(tmem + lane_base + sbuf * Hq, sv);
           tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < G; ++i) x[i] = valid ? (HKV == 2 && hi ? sv[G + i] : sv[i]) * sl2 : kNegInf;
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < G; ++i) x[i] = kNegInf;
+      }
+      // tile maximum per q head over the rows of its KV head
+      float mxs[G];
+      if constexpr (HKV == 8) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          float mx = x[i];
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          mxs[i] = mx;
+        }
+      } else {
+        float v[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) v[i] = x[i];
+        xreduce<G, true>(v);                     // lane l: the warp's maximum of q head l
+        C.xr[warp][lane] = v[0];
+        named_bar(1, 128);
+#pragma unroll
+        for (int i = 0; i < G; i += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(&C.xr[0][g * G + i]);
+          const float4 b = *reinterpret_cast<const float4*>(&C.xr[1][g * G + i]);
+          const float4 c = *reinterpret_cast<const float4*>(&C.xr[2][g * G + i]);
+          const float4 d = *reinterpret_cast<const float4*>(&C.xr[3][g * G + i]);
+          mxs[i] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+          mxs[i + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+          mxs[i + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+          mxs[i + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+        }
+      }
+      if (good) {
         float pv[G], alpha[G];
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-          const float x = valid ? (hi ? sv[G + i] : sv[i]) * sl2 : kNegInf;
-          float mx = x;
-#pragma unroll
-          for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          // every block of a split holds at least one valid token, so mx is finite
+          const float mx = mxs[i];
+          // every tile of a segment holds at least one valid key, so mx is finite
           const bool need = mx > m[i] + 8.f;
           alpha[i] = need ? ex2(m[i] - mx) : 1.f;
           m[i] = need ? mx : m[i];
           need_any |= need;
-          pv[i] = ex2(x - m[i]);
+          pv[i] = ex2(x[i] - m[i]);
           lp[i] = lp[i] * alpha[i] + pv[i];
         }
         good = wwait(P, C, &C.p_empty[sb], ((sc >> 1) & 1) ^ 1);
@@ -711,14 +821,26 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
     // goes straight on to the next segment (its PVs use the other O buffer)
     const int e = it & 1;
     good = wwait(P, C, &C.ep_empty[e], ((it >> 1) & 1) ^ 1);
+    if constexpr (HKV == 8) {
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float l = lp[i];
+      for (int i = 0; i < G; ++i) {
+        float l = lp[i];
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (good && tok == 0) {
+          C.ep[e].lsum[h0 + i] = l;
+          C.ep[e].mmax[h0 + i] = m[i];
+        }
+      }
+    } else {
+      // row sums over the four warps: lane l of each warp holds q head l's share
+      xreduce<G, false>(lp);
+      C.xr[warp][lane] = lp[0];
+      named_bar(1, 128);
+      if (good && tid < 32) C.ep[e].lsum[tid] = (C.xr[0][tid] + C.xr[1][tid]) + (C.xr[2][tid] + C.xr[3][tid]);
       if (good && tok == 0) {
-        C.ep[e].lsum[h0 + i] = l;
-        C.ep[e].mmax[h0 + i] = m[i];
+#pragma unroll
+        for (int i = 0; i < G; ++i) C.ep[e].mmax[h0 + i] = m[i];
       }
     }
     if (good && tid == 0) {
@@ -741,9 +863,9 @@ __device__ void b_softmax(const StepParams& P, Tiles<G>& T, Ctl<G>& C, uint32_t 
 // (thread = output dimension: TMEM lane 32 * (warp % 4) + lane), free the
 // buffer, then write O/l -- or, for one split of several, the partial
 // (O, m, l) for the merge phase.
-template <int G>
-__device__ void b_epilogue(const StepParams& P, Ctl<G>& C, uint32_t tmem) {
-  constexpr int Hq = Cfg<G>::Hq;
+template <int G, int HKV>
+__device__ void b_epilogue(const StepParams& P, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x - kMergeTid0;
   const int d = 32 * (warp & 3) + lane;
@@ -801,17 +923,18 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
 // counter reaches gridDim.x.  The stores are made visible to the async proxy
 // (the TMA loads of the producers) on both sides of the counter.  Not inlined:
 // the copy loop's registers stay out of the pipeline's allocation.
-static __device__ __noinline__ void append_store(const AppendParams& Ap, int64_t n_slots, unsigned int* err) {
+static __device__ __noinline__ void append_store(const AppendParams& Ap, int64_t n_slots, int n_kv_heads,
+                                                 unsigned int* err) {
   const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i0 >= (int64_t)Ap.n_tokens * kHkv * 16) return;    // no piece for this thread: nothing to fence
-  append_pieces(Ap.k_new, Ap.v_new, Ap.slots, Ap.n_tokens, Ap.k_cache, Ap.v_cache, n_slots, kHkv, 16, err, i0,
+  if (i0 >= (int64_t)Ap.n_tokens * n_kv_heads * 16) return;    // no piece for this thread: nothing to fence
+  append_pieces(Ap.k_new, Ap.v_new, Ap.slots, Ap.n_tokens, Ap.k_cache, Ap.v_cache, n_slots, n_kv_heads, 16, err, i0,
                 (int64_t)gridDim.x * blockDim.x);
   fence_proxy_async_global();
   __threadfence();
 }
 __device__ __forceinline__ void append_phase(const StepParams& P, const AppendParams& Ap) {
   if (Ap.n_tokens == 0) return;
-  append_store(Ap, (int64_t)P.num_blocks * kBlockSize, P.err);
+  append_store(Ap, (int64_t)P.num_blocks * kBlockSize, P.n_kv_heads, P.err);
   __syncthreads();
   if (threadIdx.x == 0) atomicAdd(P.queue + 2, 1);
 }
@@ -861,9 +984,9 @@ __device__ __forceinline__ void release_counters(const StepParams& P) {
 // Lane = 4 output dimensions; eight splits' loads in flight.  All threads of
 // the CTA call it; red: nw * 128 floats of shared memory that nothing else
 // uses any more (the tile rings).
-template <int G>
-__device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* slot, float* red) {
-  constexpr int Hq = Cfg<G>::Hq;
+template <int G, int HKV>
+__device__ void merge_phase(const StepParams& P, Ctl<G, HKV>& C, const int* slot, float* red) {
+  constexpr int Hq = Cfg<G, HKV>::Hq;
   const unsigned FULL = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!C.split_any) return;        // every output was written by its only split
@@ -982,22 +1105,22 @@ __device__ void merge_phase(const StepParams& P, Ctl<G>& C, const int* slot, flo
 // takes chunk b without the counter (the mixed launch's CTAs enter after
 // prefill shares of different lengths and claim every chunk).
 // TMEM columns [tmem, tmem + 5 Hq) must be allocated to the CTA.
-template <int G>
+template <int G, int HKV>
 __device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                             const CUtensorMap* qmap, Tiles<G>& T, Ctl<G>& C, const int* bpre, const int* slot,
+                             const CUtensorMap* qmap, Tiles<G, HKV>& T, Ctl<G, HKV>& C, const int* bpre, const int* slot,
                              uint32_t tmem, bool static_first) {
   const int warp = threadIdx.x >> 5;
   if (warp == 4) {
-    b_producer<G>(P, kmap, qmap, T, C, bpre, slot, static_first);
+    b_producer<G, HKV>(P, kmap, qmap, T, C, bpre, slot, static_first);
   } else if (warp == 6) {
-    v_producer<G>(P, vmap, T, C);
+    v_producer<G, HKV>(P, vmap, T, C);
   } else if (warp >= 7) {
-    b_epilogue<G>(P, C, tmem);
+    b_epilogue<G, HKV>(P, C, tmem);
   } else if (warp == 5) {
-    if ((threadIdx.x & 31) == 0) b_mma<G>(P, T, C, tmem);
+    if ((threadIdx.x & 31) == 0) b_mma<G, HKV>(P, T, C, tmem);
     __syncwarp();
   } else {
-    b_softmax<G>(P, T, C, tmem);
+    b_softmax<G, HKV>(P, T, C, tmem);
   }
 }
 

@@ -39,6 +39,7 @@ struct StepParams {
   int n_q_heads;
   int n_kv_heads;
   float scale_log2;             // scale * log2(e): scores kept in the base-2 domain
+  int window;                   // rolling window W: a query at position p sees keys p-W+1..p (0: no window)
   int split_blocks;             // decode split size (blocks)
   int max_splits_total;         // capacity of the partial buffers (splits)
   // workspace
@@ -97,8 +98,9 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int64_t
                              unsigned int* err, cudaStream_t stream);
 cudaError_t launch_decode(const StepParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int head_dim,
                           int group, int n_sms, cudaStream_t stream);
-// Decode with one block of all 8 KV heads per tensor-core tile; the cache maps
-// must have 128-row boxes and the q map a box of one token's Hq heads.  It
+// Decode with 128-row tensor-core tiles of whole blocks (8 KV heads: one block;
+// 2 or 1 KV heads with 32 query heads: 4 or 8 blocks); the cache maps must have
+// boxes of one block (16 x Hkv rows) and the q map a box of one token's Hq heads.  It
 // cuts the work into equal pieces itself (p.split_blocks is not used); the
 // partial buffers must hold n_reqs * (ceil(max blocks / 8) + 1) splits.
 cudaError_t launch_decode_tcb(const StepParams& p, const AppendParams& ap, const CUtensorMap& kmap,

@@ -62,7 +62,7 @@ struct PrefillTiles {
   uint8_t v[2][kHalves][128][128];                             // value ring
 };
 
-struct MixedCtl {
+struct alignas(16) MixedCtl {     // 16-byte multiple: the decode phase's control block follows it
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];        // per query tile (A, B)
@@ -80,9 +80,15 @@ struct MixedCtl {
   long long scan[12];
 };
 
+// Key tiles [jlo, nkt) of the pair: jlo > 0 only under a rolling window, whose
+// earliest row (position ctx + tok_lo) sees keys from ctx + tok_lo - W + 1 on.
 struct PreItem {
-  int r, g, q0, ctx, tok_lo, tok_hi, kv_hi, nkt;
+  int r, g, q0, ctx, tok_lo, tok_hi, kv_hi, nkt, jlo;
 };
+
+__device__ __forceinline__ int first_key_tile(int ctx, int tok_lo, int window) {
+  return window > 0 ? max(0, ctx + tok_lo - window + 1) / kTileN : 0;
+}
 
 // Item -> (request, KV head, token range of the tile pair).  Pairs of the same
 // request are numbered from its last tokens (most keys) down.
@@ -100,20 +106,22 @@ __device__ __forceinline__ PreItem pre_item(const StepParams& P, const int* pre,
   I.tok_hi = min(q_len, I.tok_lo + tok_per_pair);
   I.kv_hi = I.ctx + I.tok_hi;
   I.nkt = (I.kv_hi + kTileN - 1) / kTileN;
+  I.jlo = first_key_tile(I.ctx, I.tok_lo, P.window);
   return I;
 }
 
 // Key tiles of tile pair pr of a request with ctx stored and q_len new tokens.
-__device__ __forceinline__ int pair_tiles(int ctx, int q_len, int pr, int tok_per_pair) {
+__device__ __forceinline__ int pair_tiles(int ctx, int q_len, int pr, int tok_per_pair, int window) {
   const int tok_hi = min(q_len, (pr + 1) * tok_per_pair);
-  return (ctx + tok_hi + kTileN - 1) / kTileN;
+  return (ctx + tok_hi + kTileN - 1) / kTileN - first_key_tile(ctx, pr * tok_per_pair, window);
 }
 // Key tiles of all of request r's prefill items (every KV head).
 __device__ __forceinline__ long long request_tiles(const StepParams& P, int r, int tok_per_pair) {
   const int q0 = __ldg(P.cu_q_lens + r), q_len = __ldg(P.cu_q_lens + r + 1) - q0, ctx = __ldg(P.ctx_lens + r);
   if (q_len <= 1 || ctx < 0) return 0;
   long long t = 0;
-  for (int pr = 0, n = (q_len + tok_per_pair - 1) / tok_per_pair; pr < n; ++pr) t += pair_tiles(ctx, q_len, pr, tok_per_pair);
+  for (int pr = 0, n = (q_len + tok_per_pair - 1) / tok_per_pair; pr < n; ++pr)
+    t += pair_tiles(ctx, q_len, pr, tok_per_pair, P.window);
   return t * P.n_kv_heads;
 }
 
@@ -134,15 +142,15 @@ struct PieceIter {
     I = pre_item(P, pre, item, tok_per_pair);
     ++k;
     if (balanced) {
-      a = j0;
-      b = min(I.nkt, j0 + left);
+      a = I.jlo + j0;
+      b = min(I.nkt, a + left);
       ustart = u;
       u += b - a;
       left -= b - a;
       ++item;
       j0 = 0;
     } else {
-      a = 0;
+      a = I.jlo;
       b = I.nkt;
       ustart = 0;
       item += gridDim.x;
@@ -211,7 +219,7 @@ __device__ void prefill_plan(const StepParams& P, const PrefillSplit& S, MixedCt
           const int ctx = __ldg(P.ctx_lens + r), n_pairs = (q_len + TOK2 - 1) / TOK2;
           long long off = u0 - acc;
           for (int rem = 0; rem < n_pairs * P.n_kv_heads; ++rem) {
-            const int nkt = pair_tiles(ctx, q_len, n_pairs - 1 - rem / P.n_kv_heads, TOK2);
+            const int nkt = pair_tiles(ctx, q_len, n_pairs - 1 - rem / P.n_kv_heads, TOK2, P.window);
             if (off < nkt) {
               C.pc_item = pre[r] + rem;
               C.pc_j0 = (int)off;
@@ -493,6 +501,9 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
     const int ti = I.tok_lo + side * TOK + tok_l;
     const bool valid_row = ti < I.tok_hi;
     const int pos = I.ctx + min(ti, I.tok_hi - 1);            // last key this row may see
+    // first key it may see (rolling window); key k is visible iff k - lo <= pos - lo as unsigned
+    const int lo = P.window > 0 ? max(0, pos - P.window + 1) : 0;
+    const unsigned span = (unsigned)(pos - lo);
     float m = kNegInf, l = 0.f;                               // m: running max, times scale*log2 e
     bool ok = true;
     for (int j = j0; j < j1; ++j, ++sc) {
@@ -502,7 +513,7 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
       }
       tc_fence_after();
       const int key0 = j * kTileN;
-      const bool masked_tile = key0 + kTileN - 1 > pos;
+      const bool masked_tile = key0 + kTileN - 1 > pos || key0 < lo;
       // pass 1: row max over the visible keys (two 64-column loads)
       float mt;
       {
@@ -519,7 +530,8 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
 #pragma unroll
             for (int k = 0; k < 64; k += 2) {
               const int key = key0 + h * 64 + k;
-              a[(k >> 1) & 3] = max3(a[(k >> 1) & 3], key > pos ? kNegInf : sv[k], key + 1 > pos ? kNegInf : sv[k + 1]);
+              a[(k >> 1) & 3] = max3(a[(k >> 1) & 3], (unsigned)(key - lo) > span ? kNegInf : sv[k],
+                                     (unsigned)(key + 1 - lo) > span ? kNegInf : sv[k + 1]);
             }
           }
         }
@@ -567,8 +579,8 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
           float p0 = ex2(t0), p1 = ex2(t1);
           if (masked_tile) {
             const int key = key0 + h * 64 + 2 * k;
-            p0 = key > pos ? 0.f : p0;
-            p1 = key + 1 > pos ? 0.f : p1;
+            p0 = (unsigned)(key - lo) > span ? 0.f : p0;
+            p1 = (unsigned)(key + 1 - lo) > span ? 0.f : p1;
           }
           rs2[k & 1] = fadd2(rs2[k & 1], f2(p0, p1));
           pk[k] = pack_bf16(p0, p1);
@@ -611,7 +623,7 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
       break;
     }
     tc_fence_after();
-    if (j0 > 0 || j1 < I.nkt) {
+    if (j0 > I.jlo || j1 < I.nkt) {
       // a piece of an item cut at a CTA boundary: its unnormalised O and (m, l)
       // go to this CTA's slot (2b: first piece, 2b + 1: last); the CTA that ran
       // the item's first tiles merges the pieces after the grid-wide barrier
@@ -629,7 +641,7 @@ __device__ void softmax_side(const StepParams& P, const PrefillSplit& S, Prefill
             *reinterpret_cast<float4*>(orow_p + c * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
         }
         *reinterpret_cast<float2*>(base + (size_t)kPreRows * A + (side * kTileM + row) * 2) = make_float2(m, l);
-        if (j0 == 0 && side == 0 && row == 0) {
+        if (j0 == I.jlo && side == 0 && row == 0) {
           C.own_item = pieces.item - 1;
           C.own_slot = slot;
           C.own_u = u_start;
@@ -676,7 +688,7 @@ __device__ void prefill_merge(const StepParams& P, const PrefillSplit& S, const 
   constexpr int TOK = kTileM / G, Q = A / 4;
   if (!C.pc_balanced || C.own_item < 0) return;
   const PreItem I = pre_item(P, pre, C.own_item, 2 * TOK);
-  const int c0 = blockIdx.x, c1 = (int)((C.own_u + I.nkt - 1) / C.pc_L);
+  const int c0 = blockIdx.x, c1 = (int)((C.own_u + (I.nkt - I.jlo) - 1) / C.pc_L);
   const size_t slot_floats = (size_t)kPreRows * (A + 2);
   for (int task = threadIdx.x; task < kPreRows * Q; task += blockDim.x) {
     const int row = task / Q, ch = task - row * Q;
@@ -711,32 +723,35 @@ __device__ void prefill_merge(const StepParams& P, const PrefillSplit& S, const 
 
 // Shared memory of the mixed kernel: the tile region (prefill tiles, or the
 // decode pipeline's rings in phase 2), the control blocks and the plan arrays.
-template <int A, int G, bool BT>
+template <int A, int G, bool BT, int HKV>
 struct MixedLayout {
   static constexpr size_t kRegion = sizeof(PrefillTiles<A>);
   static constexpr size_t kCtl2 = 0;
 };
-template <int G>
-struct MixedLayout<128, G, true> {
-  static constexpr size_t kRegion = sizeof(PrefillTiles<128>) > sizeof(tcb::Tiles<G>) ? sizeof(PrefillTiles<128>)
-                                                                                         : sizeof(tcb::Tiles<G>);
-  static constexpr size_t kCtl2 = sizeof(tcb::Ctl<G>);
+template <int G, int HKV>
+struct MixedLayout<128, G, true, HKV> {
+  static constexpr size_t kRegion = sizeof(PrefillTiles<128>) > sizeof(tcb::Tiles<G, HKV>)
+                                        ? sizeof(PrefillTiles<128>)
+                                        : sizeof(tcb::Tiles<G, HKV>);
+  static constexpr size_t kCtl2 = sizeof(tcb::Ctl<G, HKV>);
 };
-template <int A, int G, bool BT>
+template <int A, int G, bool BT, int HKV>
 constexpr size_t mixed_smem(int n_reqs) {
-  return 1024 + MixedLayout<A, G, BT>::kRegion + sizeof(MixedCtl) + MixedLayout<A, G, BT>::kCtl2 +
+  return 1024 + MixedLayout<A, G, BT, HKV>::kRegion + sizeof(MixedCtl) + MixedLayout<A, G, BT, HKV>::kCtl2 +
          (size_t)3 * (n_reqs + 1) * 4;
 }
 
-template <int A, int G, bool BT>
+// BT: the decode phase is the block-tile pipeline, for HKV KV heads (a
+// template parameter of that pipeline; the prefill phase reads P.n_kv_heads).
+template <int A, int G, bool BT, int HKV>
 __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     mixed_kernel(const StepParams P, const AppendParams Ap, const PrefillSplit Sp, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap,
                  const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_b,
                  const __grid_constant__ CUtensorMap vmap_b, const __grid_constant__ CUtensorMap qmap_d) {
   constexpr int TOK = kTileM / G;
-  using WS = DecWarpSmem<A, G, kDecStages>;
-  using L = MixedLayout<A, G, BT>;
+  using WS = DecWarpSmem<A, (BT ? 1 : G), kDecStages>;   // CUDA-core decode rings (unused with BT)
+  using L = MixedLayout<A, G, BT, HKV>;
   static_assert(kDecWarps * sizeof(WS) <= sizeof(PrefillTiles<A>), "decode rings must fit in the tile region");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -772,7 +787,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     C.pc_u0 = 0;
     C.own_item = -1;
     if constexpr (BT) {
-      tcb::init_ctl<G>(*reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl)));
+      tcb::init_ctl<G, HKV>(*reinterpret_cast<tcb::Ctl<G, HKV>*>(base + L::kRegion + sizeof(MixedCtl)));
       prefetch_tmap(&kmap_b);
       prefetch_tmap(&vmap_b);
       prefetch_tmap(&qmap_d);
@@ -789,7 +804,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
   }
   if constexpr (BT) {
     // prefill items per request and decode blocks per request, both in request order
-    tcb::Ctl<G>& C2 = *reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl));
+    tcb::Ctl<G, HKV>& C2 = *reinterpret_cast<tcb::Ctl<G, HKV>*>(base + L::kRegion + sizeof(MixedCtl));
     tcb::append_phase(P, Ap);      // the step's new rows, when this launch stores them
     for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) {
       pre[r] = request_work(P, r, 2 * TOK, true).pre_items;
@@ -797,7 +812,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     }
     __syncthreads();
     tcb::block_scan_excl(pre, P.n_reqs, C2.scratch);
-    tcb::finish_plan<G>(P, C2, a1, a2);
+    tcb::finish_plan<G, HKV>(P, C2, a1, a2);
     prefill_plan<2 * TOK>(P, Sp, C, pre);
     if (threadIdx.x == 0 && C.pc_balanced) C2.split_any = 1;   // the pieces' merge needs the grid-wide barrier
     tcb::append_wait(P, Ap);       // before the first TMA load of the cache
@@ -821,20 +836,20 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
   __syncthreads();
   if constexpr (BT) {
     // phase 2: the tile region becomes the decode pipeline's rings
-    tcb::Tiles<G>& T2 = *reinterpret_cast<tcb::Tiles<G>*>(base);
-    tcb::Ctl<G>& C2 = *reinterpret_cast<tcb::Ctl<G>*>(base + L::kRegion + sizeof(MixedCtl));
-    tcb::zero_p<G>(T2);
+    tcb::Tiles<G, HKV>& T2 = *reinterpret_cast<tcb::Tiles<G, HKV>*>(base);
+    tcb::Ctl<G, HKV>& C2 = *reinterpret_cast<tcb::Ctl<G, HKV>*>(base + L::kRegion + sizeof(MixedCtl));
+    tcb::zero_p<G, HKV>(T2);
     fence_proxy_async_smem();
     __syncthreads();
     tc_fence_after();
-    if (!C.abort) tcb::run_pipeline<G>(P, &kmap_b, &vmap_b, &qmap_d, T2, C2, a1, a2, tmem, false);
+    if (!C.abort) tcb::run_pipeline<G, HKV>(P, &kmap_b, &vmap_b, &qmap_d, T2, C2, a1, a2, tmem, false);
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
-    tcb::merge_phase<G>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
+    tcb::merge_phase<G, HKV>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
     if (C.pc_balanced && C2.merge_ok) prefill_merge<A, G>(P, Sp, C, pre);
     tcb::release_counters(P);
   } else {
@@ -846,17 +861,20 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     decode_worker<A, G, kDecStages, 2>(P, &kmap, &vmap, reinterpret_cast<WS*>(base)[warp], a0, a1);
   }
 }
-static_assert(mixed_smem<128, 2, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
-static_assert(mixed_smem<128, 4, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
-static_assert(mixed_smem<128, 8, true>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(sizeof(PrefillTiles<128>) % 16 == 0 && sizeof(MixedCtl) % 16 == 0, "control blocks 16-byte aligned");
+static_assert(mixed_smem<128, 2, true, 8>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 4, true, 8>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 8, true, 8>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 16, true, 2>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
+static_assert(mixed_smem<128, 32, true, 1>(kMaxReqs) <= (size_t)kSmemLimit, "shared memory");
 
-template <int A, int G, bool BT>
+template <int A, int G, bool BT, int HKV>
 cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const PrefillSplit& ps, const CUtensorMap* maps,
                            int n_sms, cudaStream_t stream) {
-  const size_t smem = mixed_smem<A, G, BT>(p.n_reqs);
+  const size_t smem = mixed_smem<A, G, BT, HKV>(p.n_reqs);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;
   if (!BT && ap.n_tokens != 0) return cudaErrorInvalidValue;   // only the cooperative launch stores rows
-  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), kSmemLimit);
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(mixed_kernel<A, G, BT, HKV>), kSmemLimit);
   if (e != cudaSuccess) return e;
   if constexpr (BT) {   // cooperative: the decode merge phase waits for every CTA
     StepParams pc = p;
@@ -865,10 +883,10 @@ cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const Pr
     void* args[] = {&pc, &apc, &psc, const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
                     const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
                     const_cast<CUtensorMap*>(&maps[4]), const_cast<CUtensorMap*>(&maps[5])};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mixed_kernel<A, G, BT>), dim3(n_sms),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(mixed_kernel<A, G, BT, HKV>), dim3(n_sms),
                                        dim3(tcb::kThreads), args, smem, stream);
   } else {
-    mixed_kernel<A, G, BT><<<n_sms, kNumThreads, smem, stream>>>(p, ap, PrefillSplit{}, maps[0], maps[1], maps[2],
+    mixed_kernel<A, G, BT, HKV><<<n_sms, kNumThreads, smem, stream>>>(p, ap, PrefillSplit{}, maps[0], maps[1], maps[2],
                                                                    maps[3], maps[4], maps[5]);
     return cudaGetLastError();
   }
@@ -878,20 +896,22 @@ cudaError_t launch_mixed_t(const StepParams& p, const AppendParams& ap, const Pr
 
 cudaError_t launch_mixed(const StepParams& p, const AppendParams& ap, const PrefillSplit& ps, const CUtensorMap* maps,
                          bool block_tiles, int head_dim, int group, int n_sms, cudaStream_t stream) {
-#define CB_MIX_CASE(A_, G_, BT_)                  \
-  if (head_dim == A_ && group == G_ && block_tiles == BT_) \
-    return launch_mixed_t<A_, G_, BT_>(p, ap, ps, maps, n_sms, stream);
-  CB_MIX_CASE(128, 2, true)
-  CB_MIX_CASE(128, 4, true)
-  CB_MIX_CASE(128, 8, true)
-  CB_MIX_CASE(128, 1, false)
-  CB_MIX_CASE(128, 2, false)
-  CB_MIX_CASE(128, 4, false)
-  CB_MIX_CASE(128, 8, false)
-  CB_MIX_CASE(64, 1, false)
-  CB_MIX_CASE(64, 2, false)
-  CB_MIX_CASE(64, 4, false)
-  CB_MIX_CASE(64, 8, false)
+#define CB_MIX_CASE(A_, G_, BT_, HKV_)                                                      \
+  if (head_dim == A_ && group == G_ && block_tiles == BT_ && (!BT_ || p.n_kv_heads == HKV_)) \
+    return launch_mixed_t<A_, G_, BT_, HKV_>(p, ap, ps, maps, n_sms, stream);
+  CB_MIX_CASE(128, 2, true, 8)
+  CB_MIX_CASE(128, 4, true, 8)
+  CB_MIX_CASE(128, 8, true, 8)
+  CB_MIX_CASE(128, 16, true, 2)
+  CB_MIX_CASE(128, 32, true, 1)
+  CB_MIX_CASE(128, 1, false, 0)
+  CB_MIX_CASE(128, 2, false, 0)
+  CB_MIX_CASE(128, 4, false, 0)
+  CB_MIX_CASE(128, 8, false, 0)
+  CB_MIX_CASE(64, 1, false, 0)
+  CB_MIX_CASE(64, 2, false, 0)
+  CB_MIX_CASE(64, 4, false, 0)
+  CB_MIX_CASE(64, 8, false, 0)
 #undef CB_MIX_CASE
   return cudaErrorInvalidValue;
 }

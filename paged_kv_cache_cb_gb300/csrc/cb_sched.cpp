@@ -39,6 +39,10 @@
 //     positions stored;
 //  g. when a running request needs a block and none is free, published
 //     prefixes are dropped (oldest first) before a request is preempted.
+//  h. with a rolling window W (cb_sched_set_window), at the end of each step a
+//     running request lets go of the blocks whose positions all lie before
+//     stored - W + 1 (its next query cannot see them); their table entries
+//     become -1.  A request publishes its prefix only while it holds all of it.
 // The request that published a prefix keeps writing its own positions into
 // the shared partial block; those slots lie past the prefix, and every other
 // holder reads them from its own copy.
@@ -70,6 +74,14 @@ struct Prefix {
 
 struct Sched {
   int num_blocks, bs, budget, max_batch;
+  int window = 0;                      // rolling window (0: none)
+  // padded batching (cb_sched_set_batching): batch size (0: continuous
+  // batching), max wait in steps (-1: static), the running batch (arrival
+  // order), its longest prompt and output, the steps it has run
+  int pad_b = 0, pad_wait = -1;
+  std::vector<int> batch;
+  int n_max = 0, o_max = 0, k = 0;
+  long long last_real = 0;             // real (not pad) tokens of the last step
   std::deque<int> free_list;
   std::vector<int> ref;                // holders of each block
   std::map<int, Prefix> prefixes;      // group -> published prefix
@@ -98,8 +110,20 @@ struct Sched {
     for (int i = 0; i < need; ++i) r.blocks.push_back(take());
   }
   void release(Req& r) {
-    for (int b : r.blocks) drop(b);
+    for (int b : r.blocks)
+      if (b >= 0) drop(b);
     r.blocks.clear();
+  }
+  // h. rolling window: let go of the blocks r's next query cannot see
+  void slide(Req& r) {
+    if (window <= 0) return;
+    const long long first_seen = (long long)r.stored - window + 1;
+    const int n = (int)std::min<long long>((long long)r.blocks.size(), std::max(0LL, first_seen) / bs);
+    for (int i = 0; i < n; ++i)
+      if (r.blocks[i] >= 0) {
+        drop(r.blocks[i]);
+        r.blocks[i] = -1;
+      }
   }
   // g. drop the oldest published prefix; false when there is none
   bool evict_prefix() {
@@ -114,6 +138,8 @@ struct Sched {
   // e. publish r's prefix if its group has none and r has stored it
   void publish(const Req& r) {
     if (r.group < 0 || r.prefix <= 0 || r.stored < r.prefix || prefixes.count(r.group)) return;
+    for (int i = 0; i < blocks_for(r.prefix); ++i)
+      if (r.blocks[i] < 0) return;       // part of it already left the window
     Prefix px;
     px.tokens = r.prefix;
     px.order = n_published++;
@@ -183,6 +209,21 @@ cb_sched* cb_sched_create(int num_blocks, int block_size, int token_budget, int 
 
 void cb_sched_destroy(cb_sched* h) { delete h; }
 
+int cb_sched_set_batching(cb_sched* h, int batch_size, int max_wait) {
+  if (!h || batch_size < 1 || batch_size > h->s.max_batch || max_wait < -1 || h->s.now != 0) return CB_EINVAL;
+  h->s.pad_b = batch_size;
+  h->s.pad_wait = max_wait;
+  return CB_OK;
+}
+
+long long cb_sched_last_real_tokens(const cb_sched* h) { return h ? h->s.last_real : 0; }
+
+int cb_sched_set_window(cb_sched* h, int window) {
+  if (!h || window < 0 || h->s.now != 0) return CB_EINVAL;
+  h->s.window = window;
+  return CB_OK;
+}
+
 int cb_sched_add_request_prefix(cb_sched* h, int arrival_step, int prompt_len, int output_len, int group,
                                 int prefix_len) {
   if (!h || arrival_step < 0 || prompt_len < 1 || output_len < 1) return CB_EINVAL;
@@ -239,14 +280,113 @@ int cb_sched_request_info(const cb_sched* h, int req_id, int* produced, int* sto
 int cb_sched_kv_memory(const cb_sched* h, int max_seq_len, int64_t* out) {
   if (!h || !out || max_seq_len < 1) return CB_EINVAL;
   const Sched& s = h->s;
-  long long stored = 0;
-  for (int rid : s.running) stored += s.reqs[rid].stored;
+  long long stored = 0;                // tokens whose K/V the running requests still hold
+  for (int rid : s.running) {
+    const Req& r = s.reqs[rid];
+    stored += r.stored;
+    for (int b : r.blocks)
+      if (b < 0) stored -= s.bs;
+  }
   out[0] = (int64_t)s.running.size();
   out[1] = stored;
   out[2] = (int64_t)(s.num_blocks - (int)s.free_list.size()) * s.bs;
   out[3] = (int64_t)s.running.size() * max_seq_len;
   return CB_OK;
 }
+
+}  // extern "C"
+
+namespace {
+
+// One step of padded batching ([CB] Continuous batching: batched generation
+// with left padding; [SM] 动态批处理): a batch forms, when none runs, from the
+// waiting requests in arrival order -- at most pad_b of them, once pad_b are
+// waiting, no further request will arrive or (dynamic batching) the oldest has
+// waited pad_wait steps -- cut from its end until its padded length fits the
+// pool.  Its first step is the padded prefill (n_max positions per request);
+// then it decodes one position per request per step until the longest output
+// is done; finished requests keep decoding pads.  Blocks are taken on demand
+// and all return when the batch ends.
+int padded_step(Sched& s, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
+                int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
+                int* n_tokens_out) {
+  while (s.next_pending < s.reqs.size() && s.reqs[s.next_pending].arrival <= s.now) {
+    Req& r = s.reqs[s.next_pending++];
+    if (s.blocks_for((long long)r.prompt + r.output - 1) > s.num_blocks) {
+      r.state = kRejected;
+      continue;
+    }
+    r.state = kWaiting;
+    s.waiting.push_back(r.rid);
+  }
+  if (s.batch.empty() && !s.waiting.empty()) {
+    const bool full = (int)s.waiting.size() >= s.pad_b;
+    const bool last = s.next_pending == s.reqs.size();
+    const bool timed_out = s.pad_wait >= 0 && s.now - s.reqs[s.waiting.front()].arrival >= s.pad_wait;
+    if (full || last || timed_out) {
+      int b = std::min((int)s.waiting.size(), s.pad_b);
+      for (; b > 0; --b) {
+        int np = 0, no = 0;
+        for (int i = 0; i < b; ++i) {
+          np = std::max(np, s.reqs[s.waiting[i]].prompt);
+          no = std::max(no, s.reqs[s.waiting[i]].output);
+        }
+        if ((long long)b * s.blocks_for((long long)np + no - 1) <= s.num_blocks) {
+          s.n_max = np;
+          s.o_max = no;
+          break;
+        }
+      }
+      s.batch.assign(s.waiting.begin(), s.waiting.begin() + b);
+      s.waiting.erase(s.waiting.begin(), s.waiting.begin() + b);
+      s.k = 0;
+      for (int rid : s.batch) {
+        s.reqs[rid].state = kRunning;
+        s.running.push_back(rid);
+      }
+    }
+  }
+  int rc = 0, tok = 0;
+  long long real = 0;
+  const int nb = (int)s.batch.size();
+  // the caller's arrays hold max_batch requests and `budget` tokens
+  if (nb > s.max_batch || (long long)nb * (s.k == 0 ? s.n_max : 1) > s.budget) return CB_ESTATE;
+  cu_q_lens[0] = 0;
+  for (int i = 0; i < nb; ++i) {
+    Req& r = s.reqs[s.batch[i]];
+    const int n = s.k == 0 ? s.n_max : 1, c = s.k == 0 ? 0 : s.n_max + s.k - 1;
+    real += s.k == 0 ? r.prompt : (s.k < r.output ? 1 : 0);
+    s.grow(r, (long long)c + n);
+    req_ids[i] = r.rid;
+    q_lens[i] = n;
+    ctx_lens[i] = c;
+    cu_q_lens[i + 1] = cu_q_lens[i] + n;
+    int32_t* row = block_tables + (size_t)i * max_blocks_per_seq;
+    if ((int)r.blocks.size() > max_blocks_per_seq) rc = CB_ESTATE;
+    for (int b = 0; b < max_blocks_per_seq; ++b) row[b] = b < (int)r.blocks.size() ? r.blocks[b] : -1;
+    for (int p = c; p < c + n; ++p) slot_mapping[tok++] = (int64_t)r.blocks[p / s.bs] * s.bs + p % s.bs;
+    r.stored += n;
+    if (s.k < r.output) r.produced = std::min(r.output, s.k + 1);
+  }
+  *n_reqs_out = nb;
+  *n_tokens_out = tok;
+  s.last_real = real;
+  if (nb > 0 && ++s.k == s.o_max) {                // the longest generation is done
+    for (int rid : s.batch) {
+      Req& r = s.reqs[rid];
+      s.release(r);
+      r.state = kFinished;
+      Sched::erase(s.running, rid);
+    }
+    s.batch.clear();
+  }
+  s.now++;
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
 
 int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_lens, int32_t* cu_q_lens,
                   int32_t* block_tables, int max_blocks_per_seq, int64_t* slot_mapping, int* n_reqs_out,
@@ -256,6 +396,9 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
     return CB_EINVAL;
   Sched& s = h->s;
   s.copies.clear();
+  if (s.pad_b > 0)
+    return padded_step(s, req_ids, q_lens, ctx_lens, cu_q_lens, block_tables, max_blocks_per_seq, slot_mapping,
+                       n_reqs_out, n_tokens_out);
   // a. arrivals
   while (s.next_pending < s.reqs.size() && s.reqs[s.next_pending].arrival <= s.now) {
     Req& r = s.reqs[s.next_pending++];
@@ -372,6 +515,7 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
   }
   *n_reqs_out = nb;
   *n_tokens_out = tok;
+  s.last_real = tok;                             // no pads in continuous batching
 
   // the forward pass runs here; every scheduled request advances
   for (const Item& it : sched) {
@@ -383,6 +527,8 @@ int cb_sched_step(cb_sched* h, int32_t* req_ids, int32_t* q_lens, int32_t* ctx_l
       r.state = kFinished;
       s.release(r);
       Sched::erase(s.running, it.rid);
+    } else {
+      s.slide(r);                                // h.
     }
   }
   s.now++;

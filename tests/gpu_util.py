@@ -27,11 +27,12 @@ def cu_of(q_lens):
 
 
 def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True, attn_tables=None, fused=False,
-                slots=None):
+                slots=None, window=None):
     """Append the step's new K/V and run attention; returns (out, k_cache, v_cache, status).
     ``attn_tables`` replaces the block tables that attention reads (the append
     still uses the slots of ``inp["block_tables"]``, or ``slots`` if given).
-    ``fused``: one cb_kv_append_paged_attention call instead of the two."""
+    ``fused``: one cb_kv_append_paged_attention call instead of the two.
+    ``window``: the rolling-window entry points with this window."""
     lib = L()
     scale = scale if scale is not None else 1.0 / math.sqrt(shape.head_dim)
     if slots is None:
@@ -52,8 +53,13 @@ def device_step(shape, inp, dev="cuda", scale=None, ws_extra=0, check=True, attn
     out = torch.full_like(q, float("nan"))
     meta = (q, torch.from_numpy(cu_of(shape.q_lens)).to(dev), torch.tensor(shape.ctx_lens, dtype=torch.int32, device=dev),
             torch.from_numpy(bt).to(dev))
-    if fused:
+    if fused and window is not None:
+        lib.cb_kv_append_paged_attention_window(k_new, v_new, d_slots, *meta, k_cache, v_cache, out, scale, ws, max_q,
+                                                max_kv, window)
+    elif fused:
         lib.cb_kv_append_paged_attention(k_new, v_new, d_slots, *meta, k_cache, v_cache, out, scale, ws, max_q, max_kv)
+    elif window is not None:
+        lib.cb_paged_attention_window(*meta, k_cache, v_cache, out, scale, ws, max_q, max_kv, window)
     else:
         lib.cb_paged_attention(*meta, k_cache, v_cache, out, scale, ws, max_q, max_kv)
     status = lib.cb_last_error()
@@ -66,7 +72,7 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def oracle_step(shape, inp, scale=None):
+def oracle_step(shape, inp, scale=None, window=0):
     """fp64 oracle of the whole step: each request's stored rows read through its
     block table from the initial pool, followed by its new rows."""
     scale = scale if scale is not None else 1.0 / math.sqrt(shape.head_dim)
@@ -78,7 +84,8 @@ def oracle_step(shape, inp, scale=None):
         ks.append(np.concatenate([op.gather_request(kp, inp["block_tables"][r], c, shape.block_size), kn[t0:t0 + n]]))
         vs.append(np.concatenate([op.gather_request(vp, inp["block_tables"][r], c, shape.block_size), vn[t0:t0 + n]]))
         t0 += n
-    return oa.attention_step(q, shape.q_lens, shape.ctx_lens, ks, vs, scale, shape.n_q_heads, shape.n_kv_heads)
+    return oa.attention_step(q, shape.q_lens, shape.ctx_lens, ks, vs, scale, shape.n_q_heads, shape.n_kv_heads,
+                             window=window)
 
 
 def assert_close(got, ref, what=""):
@@ -91,7 +98,7 @@ def assert_close(got, ref, what=""):
     return err
 
 
-def sampled_request_oracle(shape, inp, r, rows=None, scale=None):
+def sampled_request_oracle(shape, inp, r, rows=None, scale=None, window=0):
     """Oracle for (some rows of) request r of a full-size step whose pool lives on
     the GPU: copy just r's physical blocks to the host, then read them through the
     oracle's gather with the table rewritten onto that compact copy."""
@@ -112,4 +119,5 @@ def sampled_request_oracle(shape, inp, r, rows=None, scale=None):
     v = np.concatenate([vc, vn])
     rows = list(range(n)) if rows is None else list(rows)
     q = f64(inp["q"][cu[r]:cu[r + 1]])[rows]
-    return oa.attention_rows(q, k, v, [c + i for i in rows], scale, shape.n_q_heads, shape.n_kv_heads), rows
+    return oa.attention_rows(q, k, v, [c + i for i in rows], scale, shape.n_q_heads, shape.n_kv_heads,
+                             window=window), rows

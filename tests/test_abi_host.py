@@ -57,7 +57,10 @@ def test_host_side_argument_checks():
         ("mq", 2), ("mkv", 40), ("kc", dummy), ("vc", dummy), ("nb", 16), ("out", dummy), ("scale", 0.1),
         ("hq", 4), ("hk", 2), ("a", 128), ("bs", 16), ("ws", dummy), ("wsb", 1 << 30), ("s", None)]]
     assert L.cb_paged_attention(*args(hq=6, hk=4)) == -1            # Hq % Hkv != 0
-    assert L.cb_paged_attention(*args(hq=32, hk=2)) == -1           # group 16 unsupported
+    assert L.cb_paged_attention(*args(hq=64, hk=4)) == -1           # group 16 only with 32 q heads on 2 KV heads
+    assert L.cb_paged_attention(*args(hq=16, hk=1)) == -1           # group 16 only with 32 q heads on 2 KV heads
+    assert L.cb_paged_attention(*args(hq=32, hk=2, a=64)) == -1     # group 16 and 32: head_dim 128 only
+    assert L.cb_paged_attention(*args(hq=64, hk=2)) == -1           # group 32 only with 1 KV head
     assert L.cb_paged_attention(*args(a=96)) == -1
     assert L.cb_paged_attention(*args(bs=8)) == -1
     assert L.cb_paged_attention(*args(nr=5000)) == -1               # more than CB_MAX_REQS

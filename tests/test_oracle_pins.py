@@ -385,3 +385,93 @@ def test_blocks_for_and_ragged_padding_zero():
     # ragged batching concatenates: the token count is the plain sum, no pad rows
     lens = [5, 1, 9]
     assert sum(lens) == sum(row.count("tok") for row in osz.left_padded_batch(lens))
+
+
+# ----------------------------------------------------------------- rolling window
+# [KVB] §Rolling KV Cache has only a heading.  Reading: a query at absolute
+# position p sees the keys p - W + 1 .. p (its own included).
+def test_window_mask_small_case_by_hand():
+    # a 3-token chunk after 2 stored tokens, W = 2: positions 2, 3, 4 see {1, 2}, {2, 3}, {3, 4}
+    want = np.array([[0, 1, 1, 0, 0], [0, 0, 1, 1, 0], [0, 0, 0, 1, 1]], dtype=bool)
+    assert np.array_equal(oa.chunk_causal_mask(3, 2, window=2), want)
+
+
+def test_window_at_least_the_context_is_no_window():
+    rng = np.random.default_rng(31)
+    q_lens, ctx_lens = [1, 5, 3], [9, 0, 4]
+    hq, hk, a = 4, 2, 8
+    q = rng.standard_normal((sum(q_lens), hq, a))
+    ks = [rng.standard_normal((c + n, hk, a)) for c, n in zip(ctx_lens, q_lens)]
+    vs = [rng.standard_normal((c + n, hk, a)) for c, n in zip(ctx_lens, q_lens)]
+    full = oa.attention_step(q, q_lens, ctx_lens, ks, vs, 0.4, hq, hk)
+    for w in (10, 11, 1000):
+        assert np.array_equal(oa.attention_step(q, q_lens, ctx_lens, ks, vs, 0.4, hq, hk, window=w), full)
+
+
+def test_window_of_one_returns_each_query_its_own_value():
+    rng = np.random.default_rng(32)
+    q_lens, ctx_lens = [1, 4], [6, 3]
+    q = rng.standard_normal((5, 2, 4))
+    ks = [rng.standard_normal((c + n, 2, 4)) for c, n in zip(ctx_lens, q_lens)]
+    vs = [rng.standard_normal((c + n, 2, 4)) for c, n in zip(ctx_lens, q_lens)]
+    got = oa.attention_step(q, q_lens, ctx_lens, ks, vs, 0.7, 2, 2, window=1)
+    assert np.allclose(got[0], vs[0][6], atol=1e-15)
+    assert np.allclose(got[1:], vs[1][3:7], atol=1e-15)
+
+
+def test_window_of_two_is_the_logistic_of_the_last_two_scores():
+    rng = np.random.default_rng(33)
+    q, k, v = rng.standard_normal((1, 1, 5)), rng.standard_normal((9, 1, 5)), rng.standard_normal((9, 1, 5))
+    got = oa.attention_step(q, [1], [8], [k], [v], 0.5, 1, 1, window=2)[0, 0]
+    d = 0.5 * (q[0, 0] @ k[8, 0] - q[0, 0] @ k[7, 0])
+    w8 = 1.0 / (1.0 + math.exp(-d))
+    assert np.allclose(got, w8 * v[8, 0] + (1 - w8) * v[7, 0], atol=1e-14)
+
+
+def test_window_brute_force_tiny_step():
+    q_lens, ctx_lens, w = [1, 4, 2], [7, 0, 5], 3
+    hq, hk, a = 4, 1, 3
+    rng = np.random.default_rng(34)
+    q = rng.standard_normal((sum(q_lens), hq, a))
+    ks = [rng.standard_normal((c + n, hk, a)) for c, n in zip(ctx_lens, q_lens)]
+    vs = [rng.standard_normal((c + n, hk, a)) for c, n in zip(ctx_lens, q_lens)]
+    got = oa.attention_step(q, q_lens, ctx_lens, ks, vs, 0.6, hq, hk, window=w)
+    t0 = 0
+    for r, (n, c) in enumerate(zip(q_lens, ctx_lens)):
+        mask = [[c + i - w < j <= c + i for j in range(c + n)] for i in range(n)]
+        for h in range(hq):
+            want = _brute_force_head(q[t0:t0 + n, h].tolist(), ks[r][:, 0].tolist(), vs[r][:, 0].tolist(), mask, 0.6)
+            assert np.allclose(got[t0:t0 + n, h], np.array(want), atol=1e-12)
+        t0 += n
+
+
+def test_window_row_equals_sdpa_over_its_last_keys():
+    """A query at position p with window W is plain (unmasked) attention over
+    keys p - W + 1 .. p: torch's SDPA in fp64 on that slice."""
+    rng = np.random.default_rng(35)
+    n, c, w, hq, hk, a = 6, 40, 9, 4, 2, 16
+    q = rng.standard_normal((n, hq, a))
+    k, v = rng.standard_normal((c + n, hk, a)), rng.standard_normal((c + n, hk, a))
+    got = oa.attention_step(q, [n], [c], [k], [v], 1 / math.sqrt(a), hq, hk, window=w)
+    for i in range(n):
+        p = c + i
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(t(q[i:i + 1]), t(k[p - w + 1:p + 1]), t(v[p - w + 1:p + 1]),
+                                             enable_gqa=True)[0].permute(1, 0, 2).numpy()
+        assert np.allclose(got[i], ref[0], atol=1e-12)
+
+
+@pytest.mark.parametrize("w", [1, 5, 16, 33])
+def test_windowed_chunks_equal_windowed_prefill(w):
+    """[CB] §Chunked prefill with the window: chunk after chunk over the stored
+    keys equals the unchunked windowed prefill, and a decode row equals the last
+    row of a windowed prefill one token longer."""
+    rng = np.random.default_rng(36 + w)
+    n, hq, hk, a = 50, 2, 1, 8
+    q, k, v = rng.standard_normal((n, hq, a)), rng.standard_normal((n, hk, a)), rng.standard_normal((n, hk, a))
+    full = oa.attention_step(q, [n], [0], [k], [v], 0.3, hq, hk, window=w)
+    for c0, c1 in [(0, 13), (13, 29), (29, 49), (49, 50)]:
+        part = oa.attention_step(q[c0:c1], [c1 - c0], [c0], [k[:c1]], [v[:c1]], 0.3, hq, hk, window=w)
+        assert np.allclose(part, full[c0:c1], atol=1e-13)
+    rows = oa.attention_rows(q[[10, 49]], k, v, [10, 49], 0.3, hq, hk, window=w)
+    assert np.allclose(rows, full[[10, 49]], atol=1e-13)

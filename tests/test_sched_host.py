@@ -17,14 +17,15 @@ def _L():
     return L
 
 
-def _compare(tr, max_batch=None, max_steps=200000, free=None):
+def _compare(tr, max_batch=None, max_steps=200000, free=None, window=0):
     L = _L()
     free = wl.free_order(tr.num_blocks, tr.seed) if free is None else free
-    o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free, max_batch=max_batch)
+    o = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks, free, max_batch=max_batch,
+                      window=window)
     maxblk = max(-(-(t[1] + t[2] - 1) // tr.block_size) for t in tr.requests)
     mb = max_batch or tr.token_budget
     maxlen = max(t[1] + t[2] - 1 for t in tr.requests)
-    s = L.Scheduler(tr.num_blocks, tr.block_size, tr.token_budget, mb, free, maxblk)
+    s = L.Scheduler(tr.num_blocks, tr.block_size, tr.token_budget, mb, free, maxblk, window=window)
     for t in tr.requests:
         s.add_request(*t)
     n = 0
@@ -172,3 +173,45 @@ def test_scheduler_memory_and_copies_argument_checks():
     s.step()                                                      # the second request takes a copy of the partial block
     assert s.step_copies().shape == (1, 2)
     assert lib.cb_sched_step_copies(s._h, None, 0) == L.CB_ESTATE   # one pair does not fit in zero
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("window", [1, 17, 40])
+def test_cpp_scheduler_rolling_window(seed, window):
+    """The rolling window's block release (tables with -1 before the window)
+    step by step, on tight traces, with and without shared prefixes."""
+    _compare(wl.small_trace(seed, num_blocks=12), window=window)
+    _compare(wl.with_prefixes(wl.small_trace(seed, num_blocks=20), 3, 9 + seed, seed=seed), window=window)
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("max_wait", [-1, 0, 3])
+def test_cpp_padded_batching_equals_oracle(seed, max_wait):
+    """Static (max_wait -1) and dynamic batching with padding: the C++ planner
+    equals oracle.scheduler.PaddedBatcher step by step, real tokens included."""
+    from oracle.scheduler import PaddedBatcher
+    L = _L()
+    tr = wl.small_trace(seed, num_blocks=40)
+    free = wl.free_order(tr.num_blocks, tr.seed)
+    B = 4
+    o = PaddedBatcher(tr.requests, B, tr.block_size, tr.num_blocks, free, max_wait=None if max_wait < 0 else max_wait)
+    maxp = max(t[1] for t in tr.requests)
+    maxblk = max(-(-(t[1] + t[2] - 1) // tr.block_size) for t in tr.requests) + -(-maxp // tr.block_size)
+    s = L.Scheduler(tr.num_blocks, tr.block_size, B * maxp, B, free, maxblk, padded_batch=B, max_wait=max_wait)
+    for t in tr.requests:
+        s.add_request(*t)
+    n = 0
+    while not o.done():
+        assert not s.done()
+        m, real = o.step()
+        g = s.step()
+        assert np.array_equal(g["req_ids"], m.req_ids), n
+        assert np.array_equal(g["q_lens"], m.q_lens), n
+        assert np.array_equal(g["ctx_lens"], m.ctx_lens), n
+        assert np.array_equal(g["slot_mapping"], m.slot_mapping), n
+        for i, tab in enumerate(m.block_tables):
+            assert g["block_tables"][i][:len(tab)].tolist() == tab
+        assert g["real_tokens"] == real, n
+        assert s.free_blocks() == len(o.free)
+        n += 1
+    assert s.done()

@@ -303,3 +303,116 @@ def test_partial_prefix_block_waits_for_a_free_block():
     assert m2.req_ids.tolist() == [2] and m2.copies == [(1, 2)]
     assert m2.block_tables == [[0, 2]] and m2.ctx_lens.tolist() == [6] and m2.q_lens.tolist() == [1]
     assert m2.slot_mapping.tolist() == [2 * 4 + 6 % 4]
+
+
+# ----------------------------------------------------------------- rolling window
+def test_rolling_window_lets_go_of_unseen_blocks_by_hand():
+    """[KVB] §Rolling KV Cache (heading only; reading: position p sees keys
+    p - W + 1 .. p).  A 40-token prompt with W = 20 in blocks of 16: after the
+    prefill the next query (position 40) sees keys 21.., so block 0 (0..15) is
+    let go (-1) and returned to the pool; block 1 (16..31) goes once the next
+    query sees keys 32.. only (after position 50 is stored)."""
+    s = FCFSScheduler([(0, 40, 20)], token_budget=64, block_size=16, num_blocks=8, free_order=range(8), window=20)
+    m0 = s.step()
+    assert m0.block_tables == [[0, 1, 2]]
+    assert s.reqs[0].blocks == [-1, 1, 2] and list(s.free) == [3, 4, 5, 6, 7, 0]
+    assert s.kv_memory(64)["stored"] == 40 - 16
+    m1 = s.step()                                  # decode position 40 into block 2
+    assert m1.block_tables == [[-1, 1, 2]] and m1.slot_mapping.tolist() == [2 * 16 + 8]
+    for _ in range(7):                             # positions 41..47
+        s.step()
+    m = s.step()                                   # position 48 opens a block: the front of the free list
+    assert m.block_tables == [[-1, 1, 2, 3]] and m.slot_mapping.tolist() == [3 * 16]
+    assert s.reqs[0].blocks == [-1, 1, 2, 3]       # stored 49: next query sees 30.., block 1 still needed
+    s.step()                                       # position 49
+    s.step()                                       # position 50: stored 51, next query sees 32..
+    assert s.reqs[0].blocks == [-1, -1, 2, 3] and list(s.free)[-1] == 1
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("window", [1, 17, 40])
+def test_rolling_window_invariants(seed, window):
+    """Every step: a running request holds exactly the blocks that hold a
+    position its next query can see (and -1 before them); free + held = pool;
+    the trace completes with every request's full output."""
+    tr = wl.small_trace(seed, num_blocks=12)
+    s = FCFSScheduler(tr.requests, tr.token_budget, tr.block_size, tr.num_blocks,
+                      wl.free_order(tr.num_blocks, tr.seed), window=window)
+    bs = tr.block_size
+    while not s.done():
+        s.step()
+        held = []
+        for r in s.running:
+            first_seen = r.stored - window + 1
+            for i, b in enumerate(r.blocks):
+                if (i + 1) * bs <= first_seen:
+                    assert b == -1, (r.rid, i)
+                else:
+                    assert b >= 0, (r.rid, i)
+                    held.append(b)
+        assert len(held) == len(set(held))
+        assert sorted(held + list(s.free)) == list(range(tr.num_blocks))
+        assert s.kv_memory(1)["stored"] == sum(min(r.stored, r.stored - (max(0, r.stored - window + 1) // bs) * bs)
+                                               for r in s.running)
+    for r in s.reqs:
+        assert r.state in ("finished", "rejected")
+        if r.state == "finished":
+            assert r.produced == r.output_len
+
+
+# ----------------------------------------------------------------- padded batching
+from oracle.scheduler import PaddedBatcher  # noqa: E402
+from oracle import sizes as osz  # noqa: E402
+
+
+def test_static_batch_by_hand():
+    """[CB] §Continuous batching (batched generation, left padding) and [SM]
+    §动态批处理: batches of 2.  Requests (arrival, prompt, output): (0,3,2),
+    (0,5,1) run first -- a padded prefill of 5 positions each (3 + 5 real
+    tokens) and one decode step (real for request 0 only).  Request 2 (arrives
+    at 1) waits for a second request, which arrives at 5; their batch pads to 4
+    positions and decodes 2 steps for request 2's 3 outputs."""
+    pb = PaddedBatcher([(0, 3, 2), (0, 5, 1), (1, 2, 3), (5, 4, 1)], batch_size=2, block_size=4, num_blocks=8,
+                       free_order=range(8))
+    steps = []
+    while not pb.done():
+        m, real = pb.step()
+        steps.append((m.req_ids.tolist(), m.q_lens.tolist(), m.ctx_lens.tolist(), real))
+    assert steps == [([0, 1], [5, 5], [0, 0], 8), ([0, 1], [1, 1], [5, 5], 1),
+                     ([], [], [], 0), ([], [], [], 0), ([], [], [], 0),
+                     ([2, 3], [4, 4], [0, 0], 6), ([2, 3], [1, 1], [4, 4], 1), ([2, 3], [1, 1], [5, 5], 1)]
+    assert sum(s[3] for s in steps) == sum(p + o - 1 for _, p, o in [(0, 3, 2), (0, 5, 1), (1, 2, 3), (5, 4, 1)])
+
+
+def test_dynamic_batch_starts_after_max_wait():
+    """Dynamic batching starts a partial batch once its oldest request has
+    waited max_wait steps: request 2 (arrival 1) runs alone at step 3."""
+    pb = PaddedBatcher([(0, 3, 2), (0, 5, 1), (1, 2, 3), (5, 4, 1)], batch_size=2, block_size=4, num_blocks=8,
+                       free_order=range(8), max_wait=2)
+    ids = []
+    while not pb.done():
+        m, _ = pb.step()
+        ids.append(m.req_ids.tolist())
+    assert ids == [[0, 1], [0, 1], [], [2], [2], [2], [3]]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_padded_prefill_pads_equal_the_left_padded_batch(seed):
+    """The padded prefill's pad positions are those of the left-padded batch
+    built by hand (oracle.sizes.left_padded_batch); every request processes
+    n_max + o_max - 1 positions; real tokens are each request's P + O - 1."""
+    tr = wl.small_trace(seed, num_blocks=60)
+    pb = PaddedBatcher(tr.requests, batch_size=4, block_size=tr.block_size, num_blocks=tr.num_blocks,
+                       free_order=wl.free_order(tr.num_blocks, tr.seed))
+    total_real = 0
+    while not pb.done():
+        batch = list(pb.batch)
+        m, real = pb.step()
+        total_real += real
+        if len(m.q_lens) and m.ctx_lens[0] == 0:            # a padded prefill
+            lens = [pb.reqs[r].prompt_len for r in m.req_ids.tolist()]
+            rows = osz.left_padded_batch(lens)
+            assert int(m.q_lens.sum()) - real == sum(row.count("pad") for row in rows)
+    done = [r for r in pb.reqs if r.state == "finished"]
+    assert total_real == sum(r.prompt_len + r.output_len - 1 for r in done)
+    assert all(r.state in ("finished", "rejected") for r in pb.reqs)

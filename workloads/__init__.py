@@ -96,6 +96,18 @@ def gqa_decode(seed=0, pool_bytes=20 * GB):
                      (1,) * len(ctx), tuple(ctx), m.seed)
 
 
+def mqa_decode(seed=0, n_kv_heads=1, n_reqs=256, ctx_lo=1024, ctx_hi=16384, pool_bytes=20 * GB):
+    """Decode-only step of a Llama-2-7B-shaped layer with multi-query attention
+    (32 query heads on 1 KV head; n_kv_heads=2: GQA groups of 16): 256 requests,
+    stored contexts uniform in [1024, 16384], so the K/V read per step (~1.1 GB
+    for one KV head) is still far larger than L2."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(ctx_lo, ctx_hi + 1, size=n_reqs)
+    name = "mqa_decode" if n_kv_heads == 1 else f"gqa{32 // n_kv_heads}_decode"
+    return StepShape(name, 32, n_kv_heads, 128, BLOCK_SIZE, pool_blocks(pool_bytes, n_kv_heads, 128),
+                     q_lens=(1,) * n_reqs, ctx_lens=tuple(int(c) for c in ctx), seed=seed)
+
+
 def long(k=15, seed=0, pool_bytes=20 * GB):
     assert 0 <= k < 16
     q = (1,) * 16 + (2048,)
@@ -260,3 +272,35 @@ def with_prefixes(tr, n_groups, prefix_len, seed=0, share=1.0):
             out.append((a, p, o, -1, 0))
     return TraceShape(tr.name + f"_prefix{n_groups}x{prefix_len}", tr.n_layers, tr.n_q_heads, tr.n_kv_heads,
                       tr.head_dim, tr.block_size, tr.token_budget, tr.num_blocks, tuple(out), tr.seed)
+
+
+@dataclass(frozen=True)
+class SequenceShape:
+    """Consecutive steps that share one KV pool and one set of block tables:
+    step k's table rows are rows of ``tables`` (request r of step k uses row
+    ``rows[k][r]``)."""
+    name: str
+    steps: tuple          # StepShape per step
+    rows: tuple           # per step, the table row of each request
+    tables: np.ndarray    # int32 [n_rows, max_blocks], -1 padded
+
+
+def long_sequence(seed=0, pool_bytes=20 * GB, n_chunks=16, chunk=2048, n_dec=16, dec_ctx=8192):
+    """The long-context workload as a sequence: a 32768-token prompt in 16
+    chunks of 2048 (step k: 2048 k stored tokens), each step co-scheduled with
+    16 decodes at 8192 + k stored tokens.  One seeded permutation of the pool
+    gives the prompt's 2048 blocks and each decode's blocks, so every step's
+    table rows are slices of the same tables."""
+    num_blocks = pool_blocks(pool_bytes, 8, 128)
+    prompt_blocks = chunk * n_chunks // BLOCK_SIZE
+    dec_blocks = -(-(dec_ctx + n_chunks) // BLOCK_SIZE)
+    assert prompt_blocks + n_dec * dec_blocks <= num_blocks, "pool too small"
+    perm = np.random.default_rng(seed + 7919).permutation(num_blocks).astype(np.int32)
+    tables = np.full((n_dec + 1, prompt_blocks), -1, np.int32)
+    for d in range(n_dec):
+        tables[d, :dec_blocks] = perm[prompt_blocks + d * dec_blocks:prompt_blocks + (d + 1) * dec_blocks]
+    tables[n_dec] = perm[:prompt_blocks]
+    steps = tuple(StepShape(f"long_seq_k{k}", 32, 8, 128, BLOCK_SIZE, num_blocks,
+                            q_lens=(1,) * n_dec + (chunk,), ctx_lens=(dec_ctx + k,) * n_dec + (chunk * k,),
+                            seed=seed + k) for k in range(n_chunks))
+    return SequenceShape("long_seq", steps, tuple(tuple(range(n_dec + 1)) for _ in steps), tables)
