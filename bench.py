@@ -756,7 +756,7 @@ def run_trace(args, world, rank, local):
         wfn = L.lib().cb_kv_append_paged_attention_window
 
         def step_fn(*x):       # the window goes after block_size
-            return wfn(*x[:20], window, *x[20:])
+            return wfn(*x[:21], window, *x[21:])
     else:
         step_fn = L.lib().cb_kv_append_paged_attention
     layer_ptrs = [(kn[i % nbuf].data_ptr(), vn[i % nbuf].data_ptr(), qn[i % nbuf].data_ptr(), kc[i].data_ptr(),
@@ -960,7 +960,7 @@ def main(argv=None):
     ap.add_argument("--trace-batching", default="continuous", choices=["continuous", "static", "dynamic"],
                     help="trace: continuous batching, or padded static / dynamic batching on the same kernels")
     ap.add_argument("--trace-batch-size", type=int, default=32, help="trace, padded batching: requests per batch")
-    ap.add_argument("--trace-max-wait", type=int, default=64, help="trace, dynamic batching: steps a request waits")
+    ap.add_argument("--trace-max-wait", type=int, default=8, help="trace, dynamic batching: steps a request waits")
     ap.add_argument("--trace-window", type=int, default=0,
                     help="trace: rolling window (keys per query; 0: none); blocks outside every window are freed")
     ap.add_argument("--trace-no-share", action="store_true",

@@ -286,12 +286,16 @@ __device__ void producer(const StepParams& P, const CUtensorMap* kmap, const CUt
     }
     if (!__shfl_sync(FULL, ok, 0)) break;
     const int nblk_hi = (I.kv_hi + kBlockSize - 1) / kBlockSize;
+    // under a rolling window, blocks wholly before the earliest row's window
+    // are seen by no row of the pair: they are not read (their table entries
+    // may already have been released) and their rows load as zeros
+    const int nblk_lo = P.window > 0 ? max(0, I.ctx + I.tok_lo - P.window + 1) / kBlockSize : 0;
     int y = rows_total;
     for (int j = j0; j < j1; ++j, ++kt) {
       if (((j - j0) & 3) == 0) {   // table entries for this tile and the next three
         const int blk = j * 8 + lane;
         y = rows_total;            // past the extent: TMA fills zeros
-        if (blk < nblk_hi) {
+        if (blk < nblk_hi && blk >= nblk_lo) {
           const int e = __ldg(P.block_tables + (size_t)I.r * P.max_blocks_per_seq + blk);
           if (e >= 0 && e < P.num_blocks)
             y = (e * Hkv + I.g) * kBlockSize;

@@ -23,24 +23,48 @@ def _bf16(rng, shape):
 
 @pytest.mark.parametrize("seed,num_blocks,head_dim,hq,hk", [(1, 16, 64, 8, 2), (2, 20, 128, 8, 2), (3, 18, 128, 32, 8)])
 def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
+    _scheduled_trace(seed, num_blocks, head_dim, hq, hk)
+
+
+@pytest.mark.parametrize("seed,num_blocks,hq,hk,window", [(4, 12, 8, 2, 24), (5, 12, 32, 8, 40), (6, 12, 32, 1, 17)])
+def test_scheduled_trace_rolling_window(seed, num_blocks, hq, hk, window):
+    """The rolling cache end to end: the scheduler lets go of blocks that left
+    every window (their table entries become -1) and hands them to other
+    requests, which overwrite them; the windowed attention never reads them."""
+    _scheduled_trace(seed, num_blocks, 128, hq, hk, window=window)
+
+
+@pytest.mark.parametrize("max_wait", [-1, 4], ids=["static", "dynamic"])
+def test_scheduled_trace_padded_batching(max_wait):
+    """Padded static / dynamic batching on the same kernels: padded prefills of
+    a whole batch and lock-step decodes, against the oracle over every position
+    (pads included: they are computed and stored like real tokens)."""
+    _scheduled_trace(7, 60, 128, 32, 8, padded=4, max_wait=max_wait)
+
+
+def _scheduled_trace(seed, num_blocks, head_dim, hq, hk, window=0, padded=0, max_wait=-1):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = L()
     tr = wl.small_trace(seed, num_blocks=num_blocks)
     a, bs, nl = head_dim, tr.block_size, 2
-    maxblk = max(-(-(p + o - 1) // bs) for _, p, o in tr.requests)
     max_seq = max(p + o - 1 for _, p, o in tr.requests)
-    sched = lib.Scheduler(tr.num_blocks, bs, tr.token_budget, tr.token_budget, wl.free_order(tr.num_blocks, tr.seed),
-                          maxblk)
+    budget, max_reqs = tr.token_budget, tr.token_budget
+    if padded:
+        max_seq = max(p for _, p, _ in tr.requests) + max(o for _, _, o in tr.requests) - 1
+        budget, max_reqs = padded * max(p for _, p, _ in tr.requests), padded
+    maxblk = -(-max_seq // bs)
+    sched = lib.Scheduler(tr.num_blocks, bs, budget, max_reqs, wl.free_order(tr.num_blocks, tr.seed), maxblk,
+                          window=window, padded_batch=padded, max_wait=max_wait)
     for arr, p, o in tr.requests:
         sched.add_request(arr, p, o)
     kc = [torch.zeros(tr.num_blocks, hk, bs, a, dtype=torch.bfloat16, device="cuda") for _ in range(nl)]
     vc = [torch.zeros_like(kc[0]) for _ in range(nl)]
-    ws = torch.empty(lib.cb_paged_attention_workspace_size(tr.token_budget, tr.token_budget, tr.token_budget, max_seq,
-                                                           hq, hk, a, bs), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(lib.cb_paged_attention_workspace_size(max_reqs, budget, budget, max_seq, hq, hk, a, bs),
+                     dtype=torch.uint8, device="cuda")
     shadow = [dict() for _ in range(nl)]          # (rid, pos) -> (k row, v row), float64
     rng = np.random.default_rng(seed)
-    steps = checked = preempted = 0
+    steps = checked = preempted = released = 0
     while not sched.done() and steps < 2000:
         m = sched.step()
         steps += 1
@@ -54,13 +78,15 @@ def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
         bt = torch.from_numpy(np.ascontiguousarray(m["block_tables"])).cuda()
         sl = torch.from_numpy(m["slot_mapping"]).cuda()
         q_lens, ctx_lens = m["q_lens"].tolist(), m["ctx_lens"].tolist()
+        released += int((m["block_tables"] == -1).sum()) - sum(
+            max(0, maxblk - -(-(c + n) // bs)) for c, n in zip(ctx_lens, q_lens))
         check = steps % 3 == 0 or m["n_preempted"] > 0
         for layer in range(nl):
             q, k, v = _bf16(rng, (t, hq, a)), _bf16(rng, (t, hk, a)), _bf16(rng, (t, hk, a))
             lib.cb_kv_append(k.cuda(), v.cuda(), sl, kc[layer], vc[layer])
             out = torch.empty(t, hq, a, dtype=torch.bfloat16, device="cuda")
-            lib.cb_paged_attention(q.cuda(), cu, ctx, bt, kc[layer], vc[layer], out, 1 / math.sqrt(a), ws,
-                                   max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens)))
+            lib.cb_paged_attention_window(q.cuda(), cu, ctx, bt, kc[layer], vc[layer], out, 1 / math.sqrt(a), ws,
+                                          max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens)), window)
             kd, vd = k.double().numpy(), v.double().numpy()
             tok = 0
             for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
@@ -72,7 +98,8 @@ def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
                 for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
                     ks.append(np.stack([shadow[layer][(rid, p)][0] for p in range(c + n)]))
                     vs.append(np.stack([shadow[layer][(rid, p)][1] for p in range(c + n)]))
-                ref = oa.attention_step(q.double().numpy(), q_lens, ctx_lens, ks, vs, 1 / math.sqrt(a), hq, hk)
+                ref = oa.attention_step(q.double().numpy(), q_lens, ctx_lens, ks, vs, 1 / math.sqrt(a), hq, hk,
+                                        window=window)
                 assert_close(out.double().cpu().numpy(), ref, f"step {steps} layer {layer}")
                 checked += 1
         assert lib.cb_last_error() == 0
@@ -80,6 +107,8 @@ def test_scheduled_trace_matches_oracle(seed, num_blocks, head_dim, hq, hk):
     assert checked > 20
     if num_blocks == 16:
         assert preempted > 0, "the tight pool is meant to exercise preemption"
+    if window:
+        assert released > 0, "the window is meant to release blocks"
 
 
 def test_full_size_trace_sampled():
