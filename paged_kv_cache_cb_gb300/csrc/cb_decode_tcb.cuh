@@ -70,7 +70,7 @@ struct Cfg {
   static_assert(HKV == 8 || HKV * G == 32, "with fewer than 8 KV heads: 32 query heads");
   static constexpr int Hq = HKV * G;
   static constexpr int BPT = 8 / HKV;                 // physical blocks per 128-row tile
-  static constexpr int KS = Hq == 64 ? 2 : 3;         // K ring stages
+  static constexpr int KS = Hq == 64 ? 2 : 3;         // K ring stages (32 KB each)
   static constexpr int VS = 2;                        // V ring stages
   static constexpr int TM = Hq <= 16 ? 128 : Hq <= 32 ? 256 : 512;   // TMEM columns: S x3, O x2, Hq each
   static constexpr int MaxW = 32 * BPT;               // most blocks in a chunk (32 tiles' worth of table entries / lanes)
@@ -728,22 +728,34 @@ __device__ void b_softmax(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C,
           mxs[i] = mx;
         }
       } else {
-        float v[G];
+        // The exact maximum matters only where it would move the reference
+        // (lazy rescale: more than 2^8 above it), so the cross-warp exchange
+        // runs only when some row of the tile has such a score -- the first
+        // tile of a segment, and rarely after; otherwise the reference stays.
+        bool grow = false;
 #pragma unroll
-        for (int i = 0; i < G; ++i) v[i] = x[i];
-        xreduce<G, true>(v);                     // lane l: the warp's maximum of q head l
-        C.xr[warp][lane] = v[0];
-        named_bar(1, 128);
+        for (int i = 0; i < G; ++i) grow |= x[i] > m[i] + 8.f;
+        if (named_bar_or(1, 128, grow)) {
+          float v[G];
 #pragma unroll
-        for (int i = 0; i < G; i += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(&C.xr[0][g * G + i]);
-          const float4 b = *reinterpret_cast<const float4*>(&C.xr[1][g * G + i]);
-          const float4 c = *reinterpret_cast<const float4*>(&C.xr[2][g * G + i]);
-          const float4 d = *reinterpret_cast<const float4*>(&C.xr[3][g * G + i]);
-          mxs[i] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
-          mxs[i + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
-          mxs[i + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
-          mxs[i + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+          for (int i = 0; i < G; ++i) v[i] = x[i];
+          xreduce<G, true>(v);                     // lane l: the warp's maximum of q head l
+          C.xr[warp][lane] = v[0];
+          named_bar(1, 128);
+#pragma unroll
+          for (int i = 0; i < G; i += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(&C.xr[0][g * G + i]);
+            const float4 b = *reinterpret_cast<const float4*>(&C.xr[1][g * G + i]);
+            const float4 c = *reinterpret_cast<const float4*>(&C.xr[2][g * G + i]);
+            const float4 d = *reinterpret_cast<const float4*>(&C.xr[3][g * G + i]);
+            mxs[i] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+            mxs[i + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+            mxs[i + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+            mxs[i + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < G; ++i) mxs[i] = m[i];
         }
       }
       if (good) {
