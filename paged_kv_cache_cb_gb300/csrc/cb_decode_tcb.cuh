@@ -21,8 +21,8 @@
 // warp leaves lane l with q head l, then shared memory).
 //
 // Work: the decode requests' blocks, laid end to end in request order and cut
-// into equal chunks of W blocks (W in [4, 32], chosen to fill the grid in the
-// fewest rounds, at most four); one CTA (11 warps) per SM, persistent, takes
+// into equal chunks of W blocks (whole tiles, up to 32 tiles' worth, chosen to
+// fill the grid in the fewest rounds, at most four); one CTA (12 warps) per SM, persistent, takes
 // chunks from a global counter (the decode kernel's CTA b starts with chunk b).  A chunk is one or more segments (request r, blocks [b0, b0+nb));
 // a request cut into several segments leaves split partials, merged by the
 // whole grid once every chunk is done.  Equal chunks keep the CTAs' finishing
@@ -38,8 +38,10 @@
 //              request's Hq query rows (one TMA box) and streams K tiles.
 //   warp 6     V producer: streams the published segments' V tiles, so a full
 //              V ring never holds up K loads (and the reverse).
-//   warp 5     MMA issuer (one lane), event driven: S(n) once K(n) lands,
-//              O += P(n) V(n) once P(n) and V(n) are ready.
+//   warp 5     S issuer (one lane), event driven: S(n) once K(n) lands.
+//   warp 11    PV issuer (one lane): O += P(n) V(n) once P(n) and V(n) are
+//              ready (two issuing threads: one thread's MMA and commit issue
+//              costs had bounded one SM's decode stream near 54 GB/s).
 //   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
 //              last PV lands and write O/l or the split partial, while the
 //              softmax warps go on with the next segment.
@@ -57,7 +59,7 @@
 namespace cb {
 namespace tcb {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kMergeTid0 = 224;   // epilogue warps 7-10
 constexpr int kChunksPerCta = 4;   // most rounds of chunks per CTA
 constexpr int kRoundBlocks = 8;    // blocks per CTA per round before a step takes another round
@@ -98,8 +100,8 @@ template <int G, int HKV = 8>
 struct alignas(16) Ctl {
   static constexpr int Hq = Cfg<G, HKV>::Hq;
   uint64_t item_full[2], item_empty[2], q_full[2], q_empty[2];
-  uint64_t k_full[Cfg<G, HKV>::KS], k_empty[Cfg<G, HKV>::KS], v_full[Cfg<G, HKV>::VS], v_empty[Cfg<G, HKV>::VS];
-  uint64_t s_full[3], p_full[2], p_empty[2], o_done[2], drain;
+  uint64_t k_full[Cfg<G, HKV>::KS], k_empty[Cfg<G, HKV>::KS], v_full[Cfg<G, HKV>::VS];
+  uint64_t s_full[3], p_full[2], o_done[2], drain, drain2;
   BItem item[2];               // the segment published in each slot (r < 0: no more work)
   int rows[2][Cfg<G, HKV>::MaxW];   // its blocks' first cache rows
   struct {
@@ -117,7 +119,7 @@ struct alignas(16) Ctl {
   int merge_ok;                // every CTA reached the merge barrier in time
   int split_any;               // some request is cut into several splits (merge phase needed)
   int W, NC, total;             // chunk size (blocks), number of chunks, blocks in all
-  int mma_nbs[4];              // MMA issuer: lengths of the segments it is between
+  int pv_issued;               // PV MMAs issued so far (the PV issuer writes, the S issuer reads)
   uint32_t tmem_base;
   volatile int abort;
   int scratch[96];
@@ -242,11 +244,10 @@ template <int G, int HKV>
 __device__ void init_ctl(Ctl<G, HKV>& C) {
   for (int s = 0; s < 2; ++s) {
     mbar_init(&C.item_full[s], 1);
-    mbar_init(&C.item_empty[s], 1 + 128 + 1);   // MMA, softmax threads, V producer
+    mbar_init(&C.item_empty[s], 2 + 128 + 1);   // both MMA issuers, softmax threads, V producer
     mbar_init(&C.q_full[s], 1);
     mbar_init(&C.q_empty[s], 1);
     mbar_init(&C.p_full[s], 128);
-    mbar_init(&C.p_empty[s], 1);
     mbar_init(&C.o_done[s], 1);
     mbar_init(&C.ep_full[s], 128);
     mbar_init(&C.ep_empty[s], 128);
@@ -259,10 +260,11 @@ __device__ void init_ctl(Ctl<G, HKV>& C) {
   }
   for (int s = 0; s < Cfg<G, HKV>::VS; ++s) {
     mbar_init(&C.v_full[s], 1);
-    mbar_init(&C.v_empty[s], 1);
   }
   for (int s = 0; s < 3; ++s) mbar_init(&C.s_full[s], 1);
   mbar_init(&C.drain, 1);
+  mbar_init(&C.drain2, 1);
+  C.pv_issued = 0;
   C.abort = 0;
   C.split_any = 0;
 }
@@ -427,7 +429,8 @@ __device__ void b_producer(const StepParams& P, const CUtensorMap* kmap, const C
       const int yb = __shfl_sync(FULL, pick<BPT>(yv, (j * BPT) >> 5), blk & 31);
       const int ks = kt % KS;
       if (lane == 0) {
-        good = lwait(P, C, &C.k_empty[ks], ((kt / KS) & 1) ^ 1);
+        // the stage is free once S of the tile that used it has completed
+        good = lwait(P, C, KS == 3 ? &C.s_full[ks] : &C.k_empty[ks], ((kt / KS) & 1) ^ 1);
         if (good) mbar_arrive_expect_tx(&C.k_full[ks], kTileBytes);
       }
       ok = __shfl_sync(FULL, good, 0);
@@ -480,7 +483,7 @@ __device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G
       const int yb = __shfl_sync(FULL, pick<BPT>(yv, (j * BPT) >> 5), blk & 31);
       const int vs = vt % VS;
       if (lane == 0) {
-        good = lwait(P, C, &C.v_empty[vs], ((vt / VS) & 1) ^ 1);
+        good = lwait(P, C, &C.o_done[vs], ((vt / VS) & 1) ^ 1);   // free once PV of its tile completed
         if (good) mbar_arrive_expect_tx(&C.v_full[vs], kTileBytes);
       }
       ok = __shfl_sync(FULL, good, 0);
@@ -495,45 +498,44 @@ __device__ void v_producer(const StepParams& P, const CUtensorMap* vmap, Tiles<G
       mbar_wait(&C.v_full[k % VS], (k / VS) & 1, 20000000ull);
 }
 
-// ---------------------------------------------------------------- MMA issuer (warp 5, one lane)
-// Event driven: S(n) = K(n) q^T is issued as soon as K(n) has landed and one of
-// the three TMEM score buffers is free (S runs at most two tiles ahead of PV);
-// O += P(n) V(n) as soon as P(n) and V(n) are ready.  A late V tile then holds
-// up only its own PV, not the K stream behind it.
+// ---------------------------------------------------------------- MMA issuers (warps 5 and 11, one lane each)
+// Two threads in different warps issue the MMAs, so their issue costs overlap:
+// the S issuer (warp 5) issues S(n) = K(n) q^T as soon as K(n) has landed and
+// one of the three TMEM score buffers is free (S runs at most two tiles ahead
+// of PV: S(n) waits until PV(n-3) was issued, which means the softmax has read
+// S(n-3) and written P(n-3)); the PV issuer (warp 11) issues O += P(n) V(n) as
+// soon as P(n) and V(n) are ready.  A late V tile then holds up only its own
+// PV, not the K stream behind it.  A tcgen05.commit covers the MMAs of the
+// issuing thread only, so each stream commits its own barriers: S(n) completes
+// s_full[n % 3] (with three K stages it also frees K stage n % 3: the K
+// producer waits on it), PV(n) completes o_done[n & 1], which also frees V
+// stage n & 1 and P buffer n & 1.  None of these waits can alias a later
+// phase: the next completion of the same barrier needs the waiter's own
+// progress first (the next K or V load, the next P).
 template <int G, int HKV>
-__device__ void b_mma(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
-  constexpr int Hq = Cfg<G, HKV>::Hq, KS = Cfg<G, HKV>::KS, VS = Cfg<G, HKV>::VS;
+__device__ void b_mma_s(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, KS = Cfg<G, HKV>::KS;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, Hq, 0, 0);
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, Hq, 0, 1);   // A = V^T: MN-major
   constexpr uint32_t kStage = (2 * 128 * 128) >> 4;              // one K/V stage, descriptor units
   constexpr uint32_t kQP = (2 * Hq * 128) >> 4;                  // one q / P buffer
-  // K, q, P: K-major, 8-row atoms 1024 B apart.  V^T: MN-major, rows (the
-  // reduction index) 128 B apart in 1024 B atoms, the two 64-dim halves 16 KB apart.
+  // K, q: K-major, 8-row atoms 1024 B apart
   const uint64_t kd0 = smem_desc_sw128(smem_u32(&T.k[0][0][0][0]), 16, 1024);
-  const uint64_t vd0 = smem_desc_sw128(smem_u32(&T.v[0][0][0][0]), 128 * 128, 1024);
   const uint64_t qd0 = smem_desc_sw128(smem_u32(&T.q[0][0][0][0]), 16, 1024);
-  const uint64_t pd0 = smem_desc_sw128(smem_u32(&T.p[0][0][0][0]), 16, 1024);
-  uint32_t ns = 0, np = 0;         // tiles whose S / PV has been issued
-  int s_it = 0, s_j = 0, s_nb = -1;   // S cursor: segment, tile in it, its length (-1: not read yet)
-  int p_it = 0, p_j = 0;           // PV cursor
-  int* nbs = C.mma_nbs;            // lengths of the segments between the cursors (by index & 3)
-  bool s_done = false, ok = true;
+  uint32_t ns = 0;                 // tiles whose S has been issued
+  int s_it = 0, s_j = 0, s_nb = -1;   // segment, tile in it, its length in tiles (-1: not read yet)
+  bool ok = true;
   uint64_t idle_since = 0;
   for (;;) {
     bool progress = false;
-    if (!s_done && s_nb < 0 && mbar_ready(&C.item_full[s_it & 1], (s_it >> 1) & 1)) {
-      const int r = C.item[s_it & 1].r, nb = C.item[s_it & 1].nt;   // tiles
+    if (s_nb < 0 && mbar_ready(&C.item_full[s_it & 1], (s_it >> 1) & 1)) {
+      const int r = C.item[s_it & 1].r, nt = C.item[s_it & 1].nt;
       mbar_arrive(&C.item_empty[s_it & 1]);
-      if (r < 0) {
-        s_done = true;
-      } else {
-        s_nb = nb;
-        nbs[s_it & 3] = nb;
-        s_j = 0;
-      }
+      if (r < 0) break;
+      s_nb = nt;
+      s_j = 0;
       progress = true;
     }
-    if (s_nb > 0 && ns < np + 3) {
+    if (s_nb > 0 && (int)ns < *(volatile int*)&C.pv_issued + 3) {
       const int sl = s_it & 1, ks = ns % KS;
       if ((s_j > 0 || mbar_ready(&C.q_full[sl], (s_it >> 1) & 1)) && mbar_ready(&C.k_full[ks], (ns / KS) & 1)) {
         tc_fence_after();
@@ -546,7 +548,7 @@ __device__ void b_mma(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uin
           tc_mma_f16(d, kd + offk, qd + offq, kIdescS, kk > 0);
         }
         tc_commit(&C.s_full[ns % 3]);
-        tc_commit(&C.k_empty[ks]);
+        if constexpr (KS != 3) tc_commit(&C.k_empty[ks]);   // with three stages s_full frees the K stage
         ++ns;
         if (++s_j == s_nb) {
           tc_commit(&C.q_empty[sl]);   // every S of this segment issued: q is free once they complete
@@ -556,31 +558,6 @@ __device__ void b_mma(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uin
         progress = true;
       }
     }
-    if (np < ns) {
-      const int pb = np & 1, vs = np % VS;
-      if (mbar_ready(&C.p_full[pb], (np >> 1) & 1) && mbar_ready(&C.v_full[vs], (np / VS) & 1) &&
-          (p_j > 0 || mbar_ready(&C.o_free[p_it & 1], ((p_it >> 1) & 1) ^ 1))) {
-        tc_fence_after();
-        const uint64_t vd = vd0 + vs * kStage, pd = pd0 + pb * kQP;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t offv = (kk * 16 * 128) >> 4;
-          const uint32_t offp = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
-          tc_mma_f16(tmem + (3 + (p_it & 1)) * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&C.o_done[np & 1]);
-        tc_commit(&C.v_empty[vs]);
-        tc_commit(&C.p_empty[pb]);
-        ++np;
-        if (++p_j == nbs[p_it & 3]) {
-          tc_commit(&C.o_full[p_it & 1]);   // the segment's O is complete once this lands
-          ++p_it;
-          p_j = 0;
-        }
-        progress = true;
-      }
-    }
-    if (s_done && np == ns) break;
     if (progress) {
       idle_since = 0;
     } else {
@@ -595,8 +572,74 @@ __device__ void b_mma(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uin
     }
   }
   if (!ok) C.abort = 1;
-  tc_commit(&C.drain);          // every MMA issued has completed before TMEM is freed
+  tc_commit(&C.drain);          // every MMA this thread issued has completed before TMEM is freed
   mbar_wait(&C.drain, 0, 20000000ull);
+}
+
+template <int G, int HKV>
+__device__ void b_mma_pv(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, VS = Cfg<G, HKV>::VS;
+  static_assert(VS == 2, "o_done[n & 1] frees V stage n % VS");
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, Hq, 0, 1);   // A = V^T: MN-major
+  constexpr uint32_t kStage = (2 * 128 * 128) >> 4;
+  constexpr uint32_t kQP = (2 * Hq * 128) >> 4;
+  // V^T: MN-major, rows (the reduction index) 128 B apart in 1024 B atoms, the
+  // two 64-dim halves 16 KB apart.  P: K-major.
+  const uint64_t vd0 = smem_desc_sw128(smem_u32(&T.v[0][0][0][0]), 128 * 128, 1024);
+  const uint64_t pd0 = smem_desc_sw128(smem_u32(&T.p[0][0][0][0]), 16, 1024);
+  uint32_t np = 0;                 // tiles whose PV has been issued
+  int p_it = 0, p_j = 0, p_nb = -1;   // segment, tile in it, its length in tiles
+  bool ok = true;
+  uint64_t idle_since = 0;
+  for (;;) {
+    bool progress = false;
+    if (p_nb < 0 && mbar_ready(&C.item_full[p_it & 1], (p_it >> 1) & 1)) {
+      const int r = C.item[p_it & 1].r, nt = C.item[p_it & 1].nt;
+      mbar_arrive(&C.item_empty[p_it & 1]);
+      if (r < 0) break;
+      p_nb = nt;
+      p_j = 0;
+      progress = true;
+    }
+    if (p_nb > 0) {
+      const int pb = np & 1, vs = np % VS;
+      if (mbar_ready(&C.p_full[pb], (np >> 1) & 1) && mbar_ready(&C.v_full[vs], (np / VS) & 1) &&
+          (p_j > 0 || mbar_ready(&C.o_free[p_it & 1], ((p_it >> 1) & 1) ^ 1))) {
+        tc_fence_after();
+        const uint64_t vd = vd0 + vs * kStage, pd = pd0 + pb * kQP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offv = (kk * 16 * 128) >> 4;
+          const uint32_t offp = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(tmem + (3 + (p_it & 1)) * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&C.o_done[np & 1]);   // also frees V stage np % 2 and P buffer np & 1
+        ++np;
+        *(volatile int*)&C.pv_issued = (int)np;   // the S issuer may reuse S buffer (np - 1) % 3
+        if (++p_j == p_nb) {
+          tc_commit(&C.o_full[p_it & 1]);   // the segment's O is complete once this lands
+          ++p_it;
+          p_nb = -1;
+        }
+        progress = true;
+      }
+    }
+    if (progress) {
+      idle_since = 0;
+    } else {
+      const uint64_t now = globaltimer_ns();
+      if (!idle_since) {
+        idle_since = now;
+      } else if (now - idle_since > kWaitLimitNs || C.abort) {
+        set_error(P.err, CB_DEVERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok) C.abort = 1;
+  tc_commit(&C.drain2);
+  mbar_wait(&C.drain2, 0, 20000000ull);
 }
 
 // n (8, 16, 32 or 64) consecutive TMEM columns of this thread's lane.
@@ -717,72 +760,73 @@ __device__ void b_softmax(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C,
 #pragma unroll
         for (int i = 0; i < G; ++i) x[i] = kNegInf;
       }
-      // tile maximum per q head over the rows of its KV head
-      float mxs[G];
-      if constexpr (HKV == 8) {
-#pragma unroll
-        for (int i = 0; i < G; ++i) {
-          float mx = x[i];
-#pragma unroll
-          for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          mxs[i] = mx;
-        }
-      } else {
-        // The exact maximum matters only where it would move the reference
-        // (lazy rescale: more than 2^8 above it), so the cross-warp exchange
-        // runs only when some row of the tile has such a score -- the first
-        // tile of a segment, and rarely after; otherwise the reference stays.
+      // With 1 or 2 KV heads a KV head's rows span the four warps.  The exact
+      // tile maximum matters only where it would move the reference (lazy
+      // rescale: more than 2^8 above it), so the cross-warp exchange runs only
+      // when some row of the tile has such a score -- the first tile of a
+      // segment, and rarely after; otherwise the reference stays.
+      bool exch = false;
+      if constexpr (HKV != 8) {
         bool grow = false;
 #pragma unroll
         for (int i = 0; i < G; ++i) grow |= x[i] > m[i] + 8.f;
-        if (named_bar_or(1, 128, grow)) {
+        exch = named_bar_or(1, 128, grow);
+        if (exch) {
           float v[G];
 #pragma unroll
           for (int i = 0; i < G; ++i) v[i] = x[i];
           xreduce<G, true>(v);                     // lane l: the warp's maximum of q head l
           C.xr[warp][lane] = v[0];
           named_bar(1, 128);
-#pragma unroll
-          for (int i = 0; i < G; i += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(&C.xr[0][g * G + i]);
-            const float4 b = *reinterpret_cast<const float4*>(&C.xr[1][g * G + i]);
-            const float4 c = *reinterpret_cast<const float4*>(&C.xr[2][g * G + i]);
-            const float4 d = *reinterpret_cast<const float4*>(&C.xr[3][g * G + i]);
-            mxs[i] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
-            mxs[i + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
-            mxs[i + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
-            mxs[i + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < G; ++i) mxs[i] = m[i];
         }
       }
+      // the P buffer is free once PV(sc - 2) has completed
+      if (good) good = wwait(P, C, &C.o_done[sb], ((sc >> 1) & 1) ^ 1);
       if (good) {
-        float pv[G], alpha[G];
+        // per q head: the tile maximum over the rows of its KV head, the
+        // running maximum (lazy rescale), p, the row sum, and p straight to P
+        const int half = tid >> 6, c = tid & 63, chunk = c >> 3, within = (c & 7) * 2;
 #pragma unroll
-        for (int i = 0; i < G; ++i) {
-          const float mx = mxs[i];
-          // every tile of a segment holds at least one valid key, so mx is finite
-          const bool need = mx > m[i] + 8.f;
-          alpha[i] = need ? ex2(m[i] - mx) : 1.f;
-          m[i] = need ? mx : m[i];
-          need_any |= need;
-          pv[i] = ex2(x[i] - m[i]);
-          lp[i] = lp[i] * alpha[i] + pv[i];
-        }
-        good = wwait(P, C, &C.p_empty[sb], ((sc >> 1) & 1) ^ 1);
-        if (good) {
-          const int half = tid >> 6, c = tid & 63, chunk = c >> 3, within = (c & 7) * 2;
+        for (int i0 = 0; i0 < G; i0 += (G >= 4 ? 4 : G)) {
+          constexpr int U = G >= 4 ? 4 : G;
+          float mxs[U];
+          if constexpr (HKV == 8) {
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
-            const int h = h0 + i;
-            *reinterpret_cast<__nv_bfloat16*>(&T.p[sb][half][h][((chunk ^ (h & 7)) << 4) + within]) =
-                __float2bfloat16_rn(pv[i]);
+            for (int u = 0; u < U; ++u) {
+              float mx = x[i0 + u];
+#pragma unroll
+              for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+              mxs[u] = mx;
+            }
+          } else {
+            static_assert(HKV == 8 || U == 4, "four heads per step");
+            if (exch) {
+              const float4 a = *reinterpret_cast<const float4*>(&C.xr[0][g * G + i0]);
+              const float4 b = *reinterpret_cast<const float4*>(&C.xr[1][g * G + i0]);
+              const float4 cc = *reinterpret_cast<const float4*>(&C.xr[2][g * G + i0]);
+              const float4 d = *reinterpret_cast<const float4*>(&C.xr[3][g * G + i0]);
+              mxs[0] = fmaxf(fmaxf(a.x, b.x), fmaxf(cc.x, d.x));
+              mxs[1] = fmaxf(fmaxf(a.y, b.y), fmaxf(cc.y, d.y));
+              mxs[2] = fmaxf(fmaxf(a.z, b.z), fmaxf(cc.z, d.z));
+              mxs[3] = fmaxf(fmaxf(a.w, b.w), fmaxf(cc.w, d.w));
+            } else {
+#pragma unroll
+              for (int u = 0; u < U; ++u) mxs[u] = m[i0 + u];
+            }
           }
-          if (tok == 0) {
 #pragma unroll
-            for (int i = 0; i < G; ++i) C.alpha[sb][h0 + i] = alpha[i];
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u, h = h0 + i;
+            // every tile of a segment holds at least one valid key, so mxs is finite
+            const bool need = mxs[u] > m[i] + 8.f;
+            const float alpha = need ? ex2(m[i] - mxs[u]) : 1.f;
+            m[i] = need ? mxs[u] : m[i];
+            need_any |= need;
+            const float pv = ex2(x[i] - m[i]);
+            lp[i] = lp[i] * alpha + pv;
+            *reinterpret_cast<__nv_bfloat16*>(&T.p[sb][half][h][((chunk ^ (h & 7)) << 4) + within]) =
+                __float2bfloat16_rn(pv);
+            if (tok == 0) C.alpha[sb][h] = alpha;
           }
         }
       }
@@ -1126,10 +1170,13 @@ __device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const
     b_producer<G, HKV>(P, kmap, qmap, T, C, bpre, slot, static_first);
   } else if (warp == 6) {
     v_producer<G, HKV>(P, vmap, T, C);
-  } else if (warp >= 7) {
+  } else if (warp >= 7 && warp <= 10) {
     b_epilogue<G, HKV>(P, C, tmem);
   } else if (warp == 5) {
-    if ((threadIdx.x & 31) == 0) b_mma<G, HKV>(P, T, C, tmem);
+    if ((threadIdx.x & 31) == 0) b_mma_s<G, HKV>(P, T, C, tmem);
+    __syncwarp();
+  } else if (warp == 11) {
+    if ((threadIdx.x & 31) == 0) b_mma_pv<G, HKV>(P, T, C, tmem);
     __syncwarp();
   } else {
     b_softmax<G, HKV>(P, T, C, tmem);

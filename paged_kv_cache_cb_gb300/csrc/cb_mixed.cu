@@ -5,10 +5,11 @@
 // prefill work (requests with more than one new token, [CB] Chunked prefill) on
 // the tensor cores; phase 2 serves the decode tokens from a global counter, so
 // CTAs that finish their prefill share early absorb more decode work.  Phase 2
-// is the block-tile pipeline of cb_decode_tcb.cuh (11 warps; one block of all
-// KV heads per MMA tile) when head_dim is 128, there are 8 KV heads and G >= 2
+// is the block-tile pipeline of cb_decode_tcb.cuh (12 warps; whole blocks of
+// every KV head per MMA tile) when head_dim is 128, there are 8 KV heads and G >= 2
+// (or 32 query heads on 1 or 2 KV heads)
 // (a cooperative launch, which may also store the step's new K/V rows first),
-// else 8 warps of the CUDA-core decode workers (11 warps in all).  The share of
+// else 8 warps of the CUDA-core decode workers (10 warps in all).  The share of
 // phase 1 is whole items round robin, or, on the cooperative launch with more
 // items than CTAs, an equal range of the items' key tiles (PieceIter): items
 // cut at CTA boundaries leave partial results that the CTA which ran their
