@@ -41,7 +41,9 @@
 //   warp 5     S issuer (one lane), event driven: S(n) once K(n) lands.
 //   warp 11    PV issuer (one lane): O += P(n) V(n) once P(n) and V(n) are
 //              ready (two issuing threads: one thread's MMA and commit issue
-//              costs had bounded one SM's decode stream near 54 GB/s).
+//              costs had bounded one SM's decode stream near 54 GB/s).  With
+//              one KV head warp 5 issues both streams from one event loop
+//              and warp 11 idles.
 //   warps 7-10 epilogue: per segment, read O (double-buffered in TMEM) once its
 //              last PV lands and write O/l or the split partial, while the
 //              softmax warps go on with the next segment.
@@ -642,6 +644,111 @@ __device__ void b_mma_pv(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, 
   mbar_wait(&C.drain2, 0, 20000000ull);
 }
 
+// One thread issuing both streams (the S issuer's and the PV issuer's steps in
+// one event loop, the same barriers and commits): used with 1 KV head (MQA),
+// where a tile's 8 rows per block are 16 TMA boxes and the softmax of 32 heads
+// per row, not MMA issue, bound the stream, and a second polling thread only
+// takes issue slots from the softmax warps (MQA decode 292 -> 241 us measured;
+// with 2 KV heads the split issuers stay 2% faster).
+template <int G, int HKV>
+__device__ void b_mma_both(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C, uint32_t tmem) {
+  constexpr int Hq = Cfg<G, HKV>::Hq, KS = Cfg<G, HKV>::KS, VS = Cfg<G, HKV>::VS;
+  static_assert(VS == 2, "o_done[n & 1] frees V stage n % VS");
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, Hq, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, Hq, 0, 1);
+  constexpr uint32_t kStage = (2 * 128 * 128) >> 4;
+  constexpr uint32_t kQP = (2 * Hq * 128) >> 4;
+  const uint64_t kd0 = smem_desc_sw128(smem_u32(&T.k[0][0][0][0]), 16, 1024);
+  const uint64_t qd0 = smem_desc_sw128(smem_u32(&T.q[0][0][0][0]), 16, 1024);
+  const uint64_t vd0 = smem_desc_sw128(smem_u32(&T.v[0][0][0][0]), 128 * 128, 1024);
+  const uint64_t pd0 = smem_desc_sw128(smem_u32(&T.p[0][0][0][0]), 16, 1024);
+  uint32_t ns = 0, np = 0;
+  int s_it = 0, s_j = 0, s_nb = -1;   // S cursor: segment, tile in it, its length in tiles
+  int p_it = 0, p_j = 0, p_nb = -1;   // PV cursor
+  bool s_done = false, ok = true;
+  uint64_t idle_since = 0;
+  for (;;) {
+    bool progress = false;
+    if (!s_done && s_nb < 0 && mbar_ready(&C.item_full[s_it & 1], (s_it >> 1) & 1)) {
+      const int r = C.item[s_it & 1].r, nt = C.item[s_it & 1].nt;
+      s_done = r < 0;
+      s_nb = s_done ? 0 : nt;         // the last item's nt is not set
+      s_j = 0;
+      progress = true;
+    }
+    if (s_nb > 0 && !s_done && ns < np + 3) {
+      const int sl = s_it & 1, ks = ns % KS;
+      if ((s_j > 0 || mbar_ready(&C.q_full[sl], (s_it >> 1) & 1)) && mbar_ready(&C.k_full[ks], (ns / KS) & 1)) {
+        tc_fence_after();
+        const uint32_t d = tmem + (ns % 3) * Hq;
+        const uint64_t kd = kd0 + ks * kStage, qd = qd0 + sl * kQP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offk = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
+          const uint32_t offq = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(d, kd + offk, qd + offq, kIdescS, kk > 0);
+        }
+        tc_commit(&C.s_full[ns % 3]);
+        if constexpr (KS != 3) tc_commit(&C.k_empty[ks]);
+        ++ns;
+        if (++s_j == s_nb) {
+          tc_commit(&C.q_empty[sl]);
+          ++s_it;
+          s_nb = -1;
+        }
+        progress = true;
+      }
+    }
+    // the PV cursor reads each segment's item after the S cursor: both arrive on item_empty
+    if (p_nb < 0 && p_it < s_it + (s_nb >= 0 ? 1 : 0)) {
+      const int r = C.item[p_it & 1].r, nt = C.item[p_it & 1].nt;
+      mbar_arrive(&C.item_empty[p_it & 1]);
+      mbar_arrive(&C.item_empty[p_it & 1]);   // both issuer arrivals (this thread stands for the two)
+      p_nb = r < 0 ? -2 : nt;                 // -2: no more segments
+      p_j = 0;
+      progress = true;
+    }
+    if (p_nb > 0 && np < ns) {
+      const int pb = np & 1, vs = np % VS;
+      if (mbar_ready(&C.p_full[pb], (np >> 1) & 1) && mbar_ready(&C.v_full[vs], (np / VS) & 1) &&
+          (p_j > 0 || mbar_ready(&C.o_free[p_it & 1], ((p_it >> 1) & 1) ^ 1))) {
+        tc_fence_after();
+        const uint64_t vd = vd0 + vs * kStage, pd = pd0 + pb * kQP;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offv = (kk * 16 * 128) >> 4;
+          const uint32_t offp = ((kk >> 2) * Hq * 128 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(tmem + (3 + (p_it & 1)) * Hq, vd + offv, pd + offp, kIdescPV, (p_j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&C.o_done[np & 1]);
+        ++np;
+        if (++p_j == p_nb) {
+          tc_commit(&C.o_full[p_it & 1]);
+          ++p_it;
+          p_nb = -1;
+        }
+        progress = true;
+      }
+    }
+    if (s_done && p_nb == -2) break;
+    if (progress) {
+      idle_since = 0;
+    } else {
+      const uint64_t now = globaltimer_ns();
+      if (!idle_since) {
+        idle_since = now;
+      } else if (now - idle_since > kWaitLimitNs || C.abort) {
+        set_error(P.err, CB_DEVERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok) C.abort = 1;
+  tc_commit(&C.drain);
+  mbar_wait(&C.drain, 0, 20000000ull);
+}
+
 // n (8, 16, 32 or 64) consecutive TMEM columns of this thread's lane.
 template <int N>
 __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
@@ -780,12 +887,12 @@ __device__ void b_softmax(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C,
           named_bar(1, 128);
         }
       }
-      // the P buffer is free once PV(sc - 2) has completed
-      if (good) good = wwait(P, C, &C.o_done[sb], ((sc >> 1) & 1) ^ 1);
       if (good) {
         // per q head: the tile maximum over the rows of its KV head, the
-        // running maximum (lazy rescale), p, the row sum, and p straight to P
-        const int half = tid >> 6, c = tid & 63, chunk = c >> 3, within = (c & 7) * 2;
+        // running maximum (lazy rescale) and its factor, p (kept as packed
+        // bf16 pairs until the P buffer is free) and the row sum.  The
+        // factors' buffer sb was last read by these threads two tiles ago.
+        uint32_t pk[(G + 1) / 2];
 #pragma unroll
         for (int i0 = 0; i0 < G; i0 += (G >= 4 ? 4 : G)) {
           constexpr int U = G >= 4 ? 4 : G;
@@ -814,19 +921,31 @@ __device__ void b_softmax(const StepParams& P, Tiles<G, HKV>& T, Ctl<G, HKV>& C,
               for (int u = 0; u < U; ++u) mxs[u] = m[i0 + u];
             }
           }
+          float pv[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const int i = i0 + u, h = h0 + i;
+            const int i = i0 + u;
             // every tile of a segment holds at least one valid key, so mxs is finite
             const bool need = mxs[u] > m[i] + 8.f;
             const float alpha = need ? ex2(m[i] - mxs[u]) : 1.f;
             m[i] = need ? mxs[u] : m[i];
             need_any |= need;
-            const float pv = ex2(x[i] - m[i]);
-            lp[i] = lp[i] * alpha + pv;
-            *reinterpret_cast<__nv_bfloat16*>(&T.p[sb][half][h][((chunk ^ (h & 7)) << 4) + within]) =
-                __float2bfloat16_rn(pv);
-            if (tok == 0) C.alpha[sb][h] = alpha;
+            pv[u] = ex2(x[i] - m[i]);
+            lp[i] = lp[i] * alpha + pv[u];
+            if (tok == 0) C.alpha[sb][h0 + i] = alpha;
+          }
+#pragma unroll
+          for (int u = 0; u < U; u += 2) pk[(i0 + u) / 2] = pack_bf16(pv[u], U > 1 ? pv[u + 1] : 0.f);
+        }
+        // the P buffer is free once PV(sc - 2) has completed
+        good = wwait(P, C, &C.o_done[sb], ((sc >> 1) & 1) ^ 1);
+        if (good) {
+          const int half = tid >> 6, c = tid & 63, chunk = c >> 3, within = (c & 7) * 2;
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            const int h = h0 + i;
+            const uint16_t hv = (uint16_t)((i & 1) ? (pk[i / 2] >> 16) : (pk[i / 2] & 0xFFFFu));
+            *reinterpret_cast<uint16_t*>(&T.p[sb][half][h][((chunk ^ (h & 7)) << 4) + within]) = hv;
           }
         }
       }
@@ -974,8 +1093,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const int* p) {
 // ---------------------------------------------------------------- fused KV append (all threads)
 // A launch given the step's new K/V rows (Ap.n_tokens > 0) stores them before
 // anything reads the cache: every thread of the grid copies its share of the
-// 16-byte pieces (append_pieces), then the CTA arrives on the grid-wide counter
-// P.queue[2].  The launch is cooperative, so all CTAs are resident and the
+// 16-byte pieces (append_pieces), and once the CTA has built its plans it
+// fences the stores and arrives on the grid-wide counter P.queue[2].  The launch is cooperative, so all CTAs are resident and the
 // counter reaches gridDim.x.  The stores are made visible to the async proxy
 // (the TMA loads of the producers) on both sides of the counter.  Not inlined:
 // the copy loop's registers stay out of the pipeline's allocation.
@@ -1173,10 +1292,16 @@ __device__ void run_pipeline(const StepParams& P, const CUtensorMap* kmap, const
   } else if (warp >= 7 && warp <= 10) {
     b_epilogue<G, HKV>(P, C, tmem);
   } else if (warp == 5) {
-    if ((threadIdx.x & 31) == 0) b_mma_s<G, HKV>(P, T, C, tmem);
+    if ((threadIdx.x & 31) == 0) {
+      if constexpr (HKV != 1)
+        b_mma_s<G, HKV>(P, T, C, tmem);
+      else
+        b_mma_both<G, HKV>(P, T, C, tmem);
+    }
     __syncwarp();
   } else if (warp == 11) {
-    if ((threadIdx.x & 31) == 0) b_mma_pv<G, HKV>(P, T, C, tmem);
+    if constexpr (HKV != 1)
+      if ((threadIdx.x & 31) == 0) b_mma_pv<G, HKV>(P, T, C, tmem);
     __syncwarp();
   } else {
     b_softmax<G, HKV>(P, T, C, tmem);
