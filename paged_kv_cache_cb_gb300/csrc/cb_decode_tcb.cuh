@@ -199,36 +199,81 @@ __device__ inline int block_scan_excl(int* a, int n, int* scratch) {
   return total;
 }
 
+// Inclusive prefix sum over a warp's lanes.
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += u;
+  }
+  return v;
+}
+
 // Given bpre[r] = decode blocks of request r (r < n), makes bpre the exclusive
 // prefix of blocks, picks the chunk size W and makes slot the prefix of splits
 // (a request spanning chunks f..l has l - f + 1).  W fills the grid in the
 // fewest rounds: R = ceil(total / (kRoundBlocks * grid)) rounds, at most
 // kChunksPerCta (more rounds balance larger steps dynamically), then
 // W = ceil(total / (R * grid)) in [kMinChunk, 32], raised if the partial
-// buffers could not hold the splits (n + chunks).  All threads call it; every
-// CTA computes the same plan.  Ends with __syncthreads().
+// buffers could not hold the splits (n + chunks).  Each thread owns a run of
+// consecutive requests; both prefix sums are warp scans whose warp totals
+// every thread adds up itself, so the plan costs three barriers.  All threads
+// call it (a whole number of warps, at most 32); every CTA computes the same
+// plan.  Ends with __syncthreads().
 template <int G, int HKV>
 __device__ void finish_plan(const StepParams& P, Ctl<G, HKV>& C, int* bpre, int* slot) {
-  const int n = P.n_reqs, tid = threadIdx.x, T = blockDim.x;
-  const int total = block_scan_excl(bpre, n, C.scratch);
+  const int n = P.n_reqs, tid = threadIdx.x, T = blockDim.x, lane = tid & 31, wid = tid >> 5, nw = T >> 5;
+  const int seg = (n + T - 1) / T, lo = min(n, tid * seg), hi = min(n, lo + seg);
+  int own = 0;                     // this thread's blocks
+  for (int i = lo; i < hi; ++i) own += bpre[i];
+  const int incl = warp_incl_scan(own);
+  if (lane == 31) C.scratch[wid] = incl;
+  __syncthreads();
+  int total = 0, run = incl - own;
+  for (int w = 0; w < nw; ++w) {
+    const int v = C.scratch[w];
+    total += v;
+    run += w < wid ? v : 0;
+  }
   constexpr int BPT = Cfg<G, HKV>::BPT;
-  const long long grid = gridDim.x;
+  const int grid = gridDim.x;
   // a round is kRoundBlocks 8-head blocks' worth of K/V per CTA: BPT blocks of fewer heads each
-  const long long rb = (long long)kRoundBlocks * BPT;
-  const long long R = max(1LL, min((long long)kChunksPerCta, (total + rb * grid - 1) / (rb * grid)));
-  long long want = (total + R * grid - 1) / (R * grid);
-  const long long cap = max(1LL, (long long)P.max_splits_total - n);   // chunks the partial buffers can take
+  const int rg = kRoundBlocks * BPT * grid;
+  const int R = max(1, min(kChunksPerCta, (total + rg - 1) / rg));
+  int want = (total + R * grid - 1) / (R * grid);
+  const int cap = max(1, P.max_splits_total - n);   // chunks the partial buffers can take
   want = max(want, (total + cap - 1) / cap);
   want = (want + BPT - 1) / BPT * BPT;           // whole tiles
-  const int W = (int)max((long long)kMinChunk, min((long long)Cfg<G, HKV>::MaxW, want));
-  for (int i = tid; i < n; i += T) {
-    const int blk = bpre[i + 1] - bpre[i];
-    slot[i] = blk > 0 ? (bpre[i] + blk - 1) / W - bpre[i] / W + 1 : 0;
-    if (slot[i] > 1) C.split_any = 1;
+  const int W = max(kMinChunk, min(Cfg<G, HKV>::MaxW, want));
+  int splits_own = 0, many = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int blk = bpre[i];
+    const int sp = blk > 0 ? (run + blk - 1) / W - run / W + 1 : 0;
+    bpre[i] = run;
+    slot[i] = sp;
+    splits_own += sp;
+    many |= sp > 1;
+    run += blk;
   }
-  __syncthreads();
-  const int splits = block_scan_excl(slot, n, C.scratch);
+  const int sincl = warp_incl_scan(splits_own);
+  if (lane == 31) C.scratch[32 + wid] = sincl;
+  many = __syncthreads_or(many);
+  int splits = 0, srun = sincl - splits_own;
+  for (int w = 0; w < nw; ++w) {
+    const int v = C.scratch[32 + w];
+    splits += v;
+    srun += w < wid ? v : 0;
+  }
+  for (int i = lo; i < hi; ++i) {
+    const int sp = slot[i];
+    slot[i] = srun;
+    srun += sp;
+  }
   if (tid == 0) {
+    bpre[n] = total;
+    slot[n] = splits;
+    if (many) C.split_any = 1;
     C.W = W;
     C.total = total;
     C.NC = (total + W - 1) / W;
