@@ -63,6 +63,8 @@ struct PrefillTiles {
   uint8_t v[2][kHalves][128][128];                             // value ring
 };
 
+constexpr int kMaxOwnItems = 2;    // whole prefill items one CTA may be dealt
+
 struct alignas(16) MixedCtl {     // 16-byte multiple: the decode phase's control block follows it
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
@@ -75,6 +77,8 @@ struct alignas(16) MixedCtl {     // 16-byte multiple: the decode phase's contro
   // starting at tile pc_j0 of item pc_item; else whole items from pc_item on
   int pc_balanced, pc_item, pc_j0, pc_len, pc_L;
   long long pc_u0;
+  // packed (pc_nown >= 0): the whole items pc_own[0 .. pc_nown), longest first
+  int pc_own[kMaxOwnItems], pc_nown;
   // the item whose first piece this CTA ran and which goes on in later CTAs
   int own_item, own_slot;
   long long own_u;
@@ -127,18 +131,25 @@ __device__ __forceinline__ long long request_tiles(const StepParams& P, int r, i
 }
 
 // A CTA's prefill pieces (item, key tiles [j0, j1)) in order.  Round robin:
-// whole items blockIdx.x, blockIdx.x + gridDim.x, ...  Balanced (the
-// cooperative launch with room for partial results): the concatenation of all
-// items' key tiles, in item order, cut into gridDim.x equal ranges of pc_L
-// units; the CTA's range may start and end inside items.
+// whole items blockIdx.x, blockIdx.x + gridDim.x, ...  Packed: the whole items
+// the plan dealt to this CTA.  Balanced (the cooperative launch with room for
+// partial results): the concatenation of all items' key tiles, in item order,
+// cut into gridDim.x equal ranges of pc_L units; the CTA's range may start and
+// end inside items.
 struct PieceIter {
-  int item, j0, left, balanced, k;
+  int item, j0, left, balanced, k, nown;
+  const int* own;                  // packed (nown >= 0): the CTA's items, in shared memory
   long long u;                     // balanced: unit at which the next piece starts
   __device__ explicit PieceIter(const MixedCtl& C)
-      : item(C.pc_item), j0(C.pc_j0), left(C.pc_len), balanced(C.pc_balanced), k(-1), u(C.pc_u0) {}
+      : item(C.pc_item), j0(C.pc_j0), left(C.pc_len), balanced(C.pc_balanced), k(-1), nown(C.pc_nown),
+        own(C.pc_own), u(C.pc_u0) {}
   // next piece into I, [a, b); piece number k (0 first); ustart: its first unit
   __device__ bool next(const StepParams& P, const int* pre, int n_pre, int tok_per_pair, PreItem& I, int& a, int& b,
                        long long& ustart) {
+    if (!balanced && nown >= 0) {
+      if (k + 1 >= nown) return false;
+      item = own[k + 1];
+    }
     if (item >= n_pre || (balanced && left <= 0)) return false;
     I = pre_item(P, pre, item, tok_per_pair);
     ++k;
@@ -154,23 +165,95 @@ struct PieceIter {
       a = I.jlo;
       b = I.nkt;
       ustart = 0;
-      item += gridDim.x;
+      if (nown < 0) item += gridDim.x;
     }
     return true;
   }
 };
 
+// Measured on GB300: one key tile of a tile pair (two 128-row query tiles
+// against 128 keys, S and PV) takes about 2.6 us of a CTA inside a full grid
+// (the long-context chunk, 1.07 TFLOP in 1.07 ms on 152 CTAs), and the decode
+// stream of a mixed step moves about 6 bytes per ns.
+constexpr long long kPairTileNs = 2600;
+constexpr long long kDecodeBytesPerNs = 6000;
+
+// Fewer items than CTAs: deal them to fewer CTAs when the step's decode stream
+// is long enough to hide it, so that more CTAs stream K/V from the start
+// instead of waiting for their one short item.  The items, longest first
+// (ties by index), go to CTAs 0 .. Np-1, then back from Np-1 to 0 (a long one
+// meets a short one); Np = ceil(n_pre / k) for the largest k <= kMaxOwnItems
+// (two: a third short item per CTA measured slower than none) whose
+// largest CTA load, at kPairTileNs per key tile with a 30 % margin, ends
+// within the decode bytes' time at kDecodeBytesPerNs.  Whole items only: no
+// partial results.  work: 2 kMaxDecodeGrid + 4 ints of free shared memory.
+// All threads call it; every CTA takes the same decision.  Ends with
+// __syncthreads().
+template <int TOK2>
+__device__ void pack_items(const StepParams& P, MixedCtl& C, const int* pre, int n_pre, long long dec_bytes,
+                           int* work) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  int* len = work;                 // key tiles of item i
+  int* order = work + kMaxDecodeGrid;   // items, longest first
+  int* mx = work + 2 * kMaxDecodeGrid;  // largest CTA load with k = 2 .. kMaxOwnItems
+  for (int i = tid; i < n_pre; i += T) {
+    const PreItem I = pre_item(P, pre, i, TOK2);
+    len[i] = I.nkt - I.jlo;
+  }
+  if (tid < kMaxOwnItems - 1) mx[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < n_pre; i += T) {
+    const int li = len[i];
+    int rank = 0;
+    for (int j = 0; j < n_pre; ++j) {
+      const int lj = len[j];
+      rank += lj > li || (lj == li && j < i);
+    }
+    order[rank] = i;
+  }
+  __syncthreads();
+  for (int k = 2; k <= kMaxOwnItems; ++k) {
+    const int np = (n_pre + k - 1) / k;
+    for (int c = tid; c < np; c += T) {
+      int load = 0;
+      for (int q = 0; q < k; ++q) {
+        const int r = q * np + ((q & 1) ? np - 1 - c : c);
+        if (r < n_pre) load += len[order[r]];
+      }
+      atomicMax(&mx[k - 2], load);
+    }
+  }
+  __syncthreads();
+  int kk = 1;
+  for (int k = kMaxOwnItems; k >= 2 && kk == 1; --k)
+    if ((long long)mx[k - 2] * kPairTileNs * 13 <= dec_bytes / kDecodeBytesPerNs * 10) kk = k;
+  if (kk > 1 && tid == 0) {
+    const int np = (n_pre + kk - 1) / kk, c = blockIdx.x;
+    int no = 0;
+    for (int q = 0; q < kk && c < np; ++q) {
+      const int r = q * np + ((q & 1) ? np - 1 - c : c);
+      if (r < n_pre) C.pc_own[no++] = order[r];
+    }
+    C.pc_nown = no;
+  }
+  __syncthreads();
+}
+
 // Plan of the balanced prefill (all threads; ends with __syncthreads()).  U =
 // all items' key tiles; CTA b runs units [b L, b L + L), L = ceil(U / grid).
 // Balanced only with room for the partials, more items than CTAs and L >= 4;
-// otherwise round robin.  Every CTA takes the same decision.
+// otherwise round robin, or the items packed onto fewer CTAs (pack_items).
+// Every CTA takes the same decision.  dec_bytes: the step's decode K/V bytes;
+// work: shared memory free until the prefill starts (pack_items).
 template <int TOK2>
-__device__ void prefill_plan(const StepParams& P, const PrefillSplit& S, MixedCtl& C, const int* pre) {
+__device__ void prefill_plan(const StepParams& P, const PrefillSplit& S, MixedCtl& C, const int* pre,
+                             long long dec_bytes, int* work) {
   const int n = P.n_reqs, T = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n_pre = pre[n];
   if (tid == 0) {
     C.pc_balanced = 0;
     C.pc_item = blockIdx.x;
+    C.pc_nown = -1;
     C.pc_j0 = 0;
     C.pc_len = 0;
     C.pc_L = 0;
@@ -179,6 +262,8 @@ __device__ void prefill_plan(const StepParams& P, const PrefillSplit& S, MixedCt
   }
   if (S.part == nullptr || S.slots < 2 * (int)gridDim.x || n_pre <= (int)gridDim.x) {
     __syncthreads();
+    if (n_pre > 1 && n_pre <= (int)gridDim.x && (int)gridDim.x <= kMaxDecodeGrid)
+      pack_items<TOK2>(P, C, pre, n_pre, dec_bytes, work);
     return;
   }
   // exclusive scan of the tiles over contiguous request segments
@@ -786,6 +871,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     C.abort = 0;
     C.pc_balanced = 0;             // prefill pieces: whole items round robin unless the plan balances them
     C.pc_item = blockIdx.x;
+    C.pc_nown = -1;
     C.pc_j0 = 0;
     C.pc_len = 0;
     C.pc_L = 0;
@@ -818,7 +904,8 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     __syncthreads();
     tcb::block_scan_excl(pre, P.n_reqs, C2.scratch);
     tcb::finish_plan<G, HKV>(P, C2, a1, a2);
-    prefill_plan<2 * TOK>(P, Sp, C, pre);
+    prefill_plan<2 * TOK>(P, Sp, C, pre, (long long)C2.total * (2 * HKV * kBlockSize * A * 2),
+                          reinterpret_cast<int*>(&T.q[0][0][0][0]));   // the tiles are free until the prefill
     if (threadIdx.x == 0 && C.pc_balanced) C2.split_any = 1;   // the pieces' merge needs the grid-wide barrier
     tcb::append_wait(P, Ap);       // before the first TMA load of the cache
   } else {

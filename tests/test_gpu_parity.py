@@ -394,6 +394,47 @@ def test_balanced_prefill_pieces_match_oracle(hq, q_lens, ctx_lens):
     _parity(shape)
 
 
+def _packed_items_per_cta(q_lens, ctx_lens, n_sms, n_kv_heads=8, tok_per_pair=64):
+    """The plan's packing rule restated: items (whole tile pairs of one KV head)
+    per CTA when there are fewer items than CTAs: k = 2 if the largest CTA
+    load (items longest first, dealt 0..Np-1, then Np-1..0) times
+    2.6 us per key tile, with a 30 % margin, fits in the decode bytes at 6 B/ns."""
+    lens, dec_blocks = [], 0
+    for q, c in zip(q_lens, ctx_lens):
+        if q == 1:
+            dec_blocks += -(-(c + 1) // 16)
+        elif q > 1:
+            for pr in range(-(-q // tok_per_pair)):
+                lens += [-(-(c + min(q, (pr + 1) * tok_per_pair)) // 128)] * n_kv_heads
+    if not 1 < len(lens) <= n_sms:
+        return 1
+    order = sorted(lens, reverse=True)
+    dec_ns = dec_blocks * 2 * n_kv_heads * 16 * 128 * 2 // 6000
+    for k in (2,):
+        np_ = -(-len(lens) // k)
+        load = max(sum(order[r] for q in range(k) for r in [q * np_ + (np_ - 1 - c if q & 1 else c)] if r < len(lens))
+                   for c in range(np_))
+        if load * 2600 * 13 <= dec_ns * 10:
+            return k
+    return 1
+
+
+@pytest.mark.parametrize("q_lens,ctx_lens,k", [
+    ((1,) * 16 + (256, 64), tuple(5200 + 37 * i for i in range(16)) + (200, 0), 2),
+    ((1,) * 16 + (512,), tuple(8000 + 11 * i for i in range(16)) + (1024,), 2),
+    ((1,) * 3 + (512,), (300, 200, 100) + (1024,), 1),
+], ids=["short_items", "one_chunk", "too_little_decode"])
+def test_prefill_items_packed_onto_fewer_ctas(q_lens, ctx_lens, k):
+    """Fewer prefill items than CTAs beside a long decode stream: the plan deals
+    whole items to fewer CTAs (longest first, a long one with a short one) so
+    that the other CTAs stream the decodes from the start; beside a short
+    decode stream they stay one per CTA.  Every row against the oracle."""
+    assert _packed_items_per_cta(q_lens, ctx_lens, torch.cuda.get_device_properties(0).multi_processor_count) == k
+    blocks = sum(-(-(c + q) // 16) for c, q in zip(ctx_lens, q_lens)) + 8
+    shape = wl.StepShape(f"packed_{k}", 32, 8, 128, 16, blocks, q_lens=q_lens, ctx_lens=ctx_lens, seed=40 + k)
+    _parity(shape)
+
+
 def test_prefill_without_room_for_pieces_keeps_pairs_whole():
     """A workspace without the partials' region: the launch keeps tile pairs whole."""
     shape = wl.StepShape("whole_pairs", 32, 8, 128, 16, 240, q_lens=(1600,), ctx_lens=(1700,), seed=5)
