@@ -10,10 +10,13 @@
 // (or 32 query heads on 1 or 2 KV heads)
 // (a cooperative launch, which may also store the step's new K/V rows first),
 // else 8 warps of the CUDA-core decode workers (10 warps in all).  The share of
-// phase 1 is whole items round robin, or, on the cooperative launch with more
-// items than CTAs, an equal range of the items' key tiles (PieceIter): items
-// cut at CTA boundaries leave partial results that the CTA which ran their
-// first tiles merges after the grid-wide barrier (prefill_merge).
+// phase 1 is whole items round robin; with fewer items than CTAs beside a long
+// decode stream, whole items packed two to a CTA on half as many CTAs (the
+// others stream decodes from the start, pack_items); or, on the cooperative
+// launch with more items than CTAs, an equal range of the items' key tiles
+// (PieceIter): items cut at CTA boundaries leave partial results that the CTA
+// which ran their first tiles merges after the grid-wide barrier
+// (prefill_merge).
 //
 // Prefill item = (request r, KV head g, pair of query tiles A and B).  A query
 // tile is 128 rows = 128/G new tokens x the G query heads of group g (GQA heads
