@@ -688,7 +688,9 @@ def run_trace(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream()
+    # a stream of its own: the legacy default stream cannot be recorded into a graph
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
     sh = stream.cuda_stream            # raw handle: the cheapest form for the per-layer calls
     tr = wl.trace(seed=args.seed + rank, pool_bytes=int(args.trace_pool_gb * wl.GB), n_layers=args.trace_layers)
     if args.trace_prefix_groups > 0:       # shared system prompts: blocks shared, partial last block copied
@@ -764,6 +766,14 @@ def run_trace(args, world, rank, local):
     fixed = dict(sl=d_sl.data_ptr(), cu=d_cu.data_ptr(), ctx=d_ctx.data_ptr(), bt=d_bt.data_ptr(),
                  out=out.data_ptr(), ws=ws.data_ptr(), wsb=ws.numel())
 
+    # Each iteration's layer calls recorded as one CUDA graph and launched at once
+    # (kernels of a graph start ~0.8 us after their predecessor instead of ~2.8
+    # us); one graph per kind of iteration, updated in place while its kernels
+    # stay the same.  A kind's first iteration runs directly: the library sets up
+    # a kernel's per-device state on its first call, outside any recording.
+    graphs, seen = {}, set()
+    use_graphs = not args.trace_eager
+
     def one_step(i, host_io=None):
         m = sched.step()
         pairs = sched.step_copies()             # copy-on-write of shared partial blocks, before the append
@@ -793,6 +803,11 @@ def run_trace(args, world, rank, local):
         hb["ev"].record(stream)
         q_lens, ctx = m["q_lens"], m["ctx_lens"]
         max_q, max_kv = int(q_lens.max()), int((q_lens + ctx).max())
+        kind = (max_q > 1, npairs > 0)
+        graph = None
+        if use_graphs and host_io is None and kind in seen:
+            graph = graphs.setdefault(kind, L.Graph())
+            graph.begin(sh)
         for layer in range(nl):
             if host_io is not None:                 # end-to-end: this step's rows come from pinned host memory
                 qn[layer][:t].copy_(host_io["q"][layer][:t], non_blocking=True)
@@ -809,6 +824,9 @@ def run_trace(args, world, rank, local):
             stats["launches"] += L.cb_last_launch_count()
             if host_io is not None:
                 host_io["out"][:t].copy_(out[:t], non_blocking=True)
+        if graph is not None:
+            graph.end(sh)
+        seen.add(kind)
         if host_io is not None:
             stats["h2d"] += nl * t * (hq + 2 * hk) * a * 2 + 4 * (2 * b + 1) + 4 * b * maxblk + 8 * t
             stats["d2h"] += nl * t * hq * a * 2
@@ -924,6 +942,9 @@ def run_trace(args, world, rank, local):
                           ", blocks shared, partial last block copied on write")
                        if args.trace_prefix_groups > 0 else ""),
                    "n_layers": nl, "num_blocks": nb, "token_budget": budget,
+                   "launch": ("per layer, directly" if args.trace_eager else
+                              "each iteration's layer calls recorded as one CUDA graph (cb_graph_begin / "
+                              "cb_graph_end, updated in place per kind of iteration); the end-to-end run directly"),
                    "decode_tokens": timed["dec"], "prefill_tokens": timed["pre"], "idle_steps": timed["idle"],
                    "preemptions": timed["preempted"],
                    "l2": "inputs larger than L2: each iteration reads every running request's K/V in 32 layers",
@@ -963,6 +984,9 @@ def main(argv=None):
     ap.add_argument("--trace-max-wait", type=int, default=8, help="trace, dynamic batching: steps a request waits")
     ap.add_argument("--trace-window", type=int, default=0,
                     help="trace: rolling window (keys per query; 0: none); blocks outside every window are freed")
+    ap.add_argument("--trace-eager", action="store_true",
+                    help="trace: launch every layer's call directly instead of recording each iteration's calls as "
+                         "one CUDA graph (cb_graph_begin / cb_graph_end)")
     ap.add_argument("--trace-no-share", action="store_true",
                     help="trace with prefix groups: compute every prompt in full (no block sharing)")
     ap.add_argument("--seed", type=int, default=0)

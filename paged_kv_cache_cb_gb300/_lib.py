@@ -44,6 +44,10 @@ SIGNATURES = [
     ("cb_strerror", ctypes.c_char_p, [_c_int]),
     ("cb_hbm_copy", _c_int, [_vp, _vp, _c_size, _vp]),
     ("cb_last_launch_count", _c_int, []),
+    ("cb_graph_create", _vp, []),
+    ("cb_graph_destroy", None, [_vp]),
+    ("cb_graph_begin", _c_int, [_vp, _vp]),
+    ("cb_graph_end", _c_int, [_vp, _vp]),
     ("cb_build_slot_mapping", _c_int, [_i32p, _i32p, _i32p, _c_int, _c_int, _c_int, _i64p]),
     ("cb_sched_create", _vp, [_c_int, _c_int, _c_int, _c_int, _i32p]),
     ("cb_sched_destroy", None, [_vp]),
@@ -328,6 +332,39 @@ def cb_build_slot_mapping(q_lens, ctx_lens, block_tables, block_size):
     rc = lib().cb_build_slot_mapping(pq, pc, pbt, bt.shape[1], q.size, int(block_size), out.ctypes.data_as(_i64p))
     _check("cb_build_slot_mapping", rc)
     return out
+
+
+class Graph:
+    """cb_graph: record the library calls made on a stream between ``begin`` and
+    ``end`` and run them as one CUDA graph (updated in place while the same
+    kernels are recorded).  ``stream`` is a raw stream handle or a
+    torch.cuda.Stream, never the legacy default stream."""
+
+    def __init__(self):
+        self._g = lib().cb_graph_create()
+        if not self._g:
+            raise CBError("cb_graph_create", CB_ECUDA)
+
+    @staticmethod
+    def _handle(stream):
+        return stream if isinstance(stream, int) else stream.cuda_stream
+
+    def begin(self, stream):
+        _check("cb_graph_begin", lib().cb_graph_begin(self._g, self._handle(stream)))
+
+    def end(self, stream):
+        _check("cb_graph_end", lib().cb_graph_end(self._g, self._handle(stream)))
+
+    def close(self):
+        if self._g:
+            lib().cb_graph_destroy(self._g)
+            self._g = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Scheduler:

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <new>
 #include <set>
 
 #include "../../include/cbattn.h"
@@ -528,5 +529,71 @@ int cb_hbm_copy(void* dst, const void* src, size_t bytes, void* stream) {
 }
 
 int cb_last_launch_count(void) { return g_last_launches; }
+
+// ---------------------------------------------------------------- graphs
+struct cb_graph {
+  cudaGraphExec_t exec = nullptr;
+  int device = -1;
+};
+
+cb_graph* cb_graph_create(void) { return new (std::nothrow) cb_graph(); }
+
+void cb_graph_destroy(cb_graph* g) {
+  if (!g) return;
+  if (g->exec) (void)cudaGraphExecDestroy(g->exec);
+  delete g;
+}
+
+int cb_graph_begin(cb_graph* g, void* stream) {
+  if (!g || !stream) return CB_EINVAL;
+  if (cudaStreamBeginCapture(static_cast<cudaStream_t>(stream), cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CB_ECUDA;
+  }
+  return CB_OK;
+}
+
+int cb_graph_end(cb_graph* g, void* stream) {
+  if (!g || !stream) return CB_EINVAL;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamEndCapture(s, &graph) != cudaSuccess || !graph) {
+    (void)cudaGetLastError();
+    if (graph) (void)cudaGraphDestroy(graph);
+    return CB_ECUDA;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGraphDestroy(graph);
+    return CB_ECUDA;
+  }
+  if (g->exec && g->device == dev) {
+    // the same kernels in the same order: new parameters in place, no instantiation
+    cudaGraphExecUpdateResultInfo info;
+    if (cudaGraphExecUpdate(g->exec, graph, &info) != cudaSuccess) {
+      (void)cudaGetLastError();
+      (void)cudaGraphExecDestroy(g->exec);
+      g->exec = nullptr;
+    }
+  } else if (g->exec) {
+    (void)cudaGraphExecDestroy(g->exec);
+    g->exec = nullptr;
+  }
+  if (!g->exec) {
+    if (cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      g->exec = nullptr;
+      (void)cudaGraphDestroy(graph);
+      return CB_ECUDA;
+    }
+    g->device = dev;
+  }
+  (void)cudaGraphDestroy(graph);
+  if (cudaGraphLaunch(g->exec, s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CB_ECUDA;
+  }
+  return CB_OK;
+}
 
 }  // extern "C"

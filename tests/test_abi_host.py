@@ -151,3 +151,20 @@ def test_binding_refuses_host_tensors():
         L.cb_kv_append_paged_attention(kn, kn, sl, q, cu, ctx, bt, kc, kc, q.clone(), 0.125, ws, 3, 8)
     with pytest.raises(ValueError, match="CUDA"):
         L.cb_copy_blocks(torch.zeros(1, 2, dtype=torch.int32), kc, kc)
+
+
+def test_graph_calls_reject_null_arguments():
+    """cb_graph_begin / cb_graph_end check their arguments before any CUDA call."""
+    L = _lib()
+    lib = L.lib()
+    g = lib.cb_graph_create()
+    assert g
+    try:
+        assert lib.cb_graph_begin(g, None) == L.CB_EINVAL      # the legacy default stream cannot be captured
+        assert lib.cb_graph_end(g, None) == L.CB_EINVAL
+        assert lib.cb_graph_begin(None, 1) == L.CB_EINVAL
+        assert lib.cb_graph_end(None, 1) == L.CB_EINVAL
+    finally:
+        lib.cb_graph_destroy(g)
+    lib.cb_graph_destroy(None)                                 # a no-op
+
