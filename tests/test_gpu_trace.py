@@ -42,10 +42,23 @@ def test_scheduled_trace_padded_batching(max_wait):
     _scheduled_trace(7, 60, 128, 32, 8, padded=4, max_wait=max_wait)
 
 
-def _scheduled_trace(seed, num_blocks, head_dim, hq, hk, window=0, padded=0, max_wait=-1):
+@pytest.mark.parametrize("seed,num_blocks,window", [(0, 40, 0), (3, 16, 0), (4, 40, 24)],
+                         ids=["ample", "tight_preempting", "window"])
+def test_scheduled_trace_recorded_as_graphs(seed, num_blocks, window):
+    _scheduled_trace(seed, num_blocks, 128, 32, 8, window=window, graphs=True)
+
+
+def _scheduled_trace(seed, num_blocks, head_dim, hq, hk, window=0, padded=0, max_wait=-1, graphs=False):
+    """A small scheduled trace through the library, every third step (and every
+    step that preempts) checked against the oracle.  graphs: each step's layer
+    calls recorded and launched as one CUDA graph (cb_graph_begin / cb_graph_end)
+    on a stream of their own, one graph object per kind of step, a kind's first
+    step run directly -- the serving loop of the benchmark's trace."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     lib = L()
+    stream = torch.cuda.Stream() if graphs else torch.cuda.current_stream()
+    recorders, seen, recorded = {}, set(), 0
     tr = wl.small_trace(seed, num_blocks=num_blocks)
     a, bs, nl = head_dim, tr.block_size, 2
     max_seq = max(p + o - 1 for _, p, o in tr.requests)
@@ -65,46 +78,65 @@ def _scheduled_trace(seed, num_blocks, head_dim, hq, hk, window=0, padded=0, max
     shadow = [dict() for _ in range(nl)]          # (rid, pos) -> (k row, v row), float64
     rng = np.random.default_rng(seed)
     steps = checked = preempted = released = 0
+    torch.cuda.synchronize()                      # the caches and workspace above, before `stream` uses them
     while not sched.done() and steps < 2000:
-        m = sched.step()
-        steps += 1
-        preempted += m["n_preempted"]
-        b = len(m["req_ids"])
-        if b == 0:
-            continue
-        t = int(m["cu_q_lens"][-1])
-        cu = torch.from_numpy(m["cu_q_lens"]).cuda()
-        ctx = torch.from_numpy(m["ctx_lens"]).cuda()
-        bt = torch.from_numpy(np.ascontiguousarray(m["block_tables"])).cuda()
-        sl = torch.from_numpy(m["slot_mapping"]).cuda()
-        q_lens, ctx_lens = m["q_lens"].tolist(), m["ctx_lens"].tolist()
-        released += int((m["block_tables"] == -1).sum()) - sum(
-            max(0, maxblk - -(-(c + n) // bs)) for c, n in zip(ctx_lens, q_lens))
-        check = steps % 3 == 0 or m["n_preempted"] > 0
-        for layer in range(nl):
-            q, k, v = _bf16(rng, (t, hq, a)), _bf16(rng, (t, hk, a)), _bf16(rng, (t, hk, a))
-            lib.cb_kv_append(k.cuda(), v.cuda(), sl, kc[layer], vc[layer])
-            out = torch.empty(t, hq, a, dtype=torch.bfloat16, device="cuda")
-            lib.cb_paged_attention_window(q.cuda(), cu, ctx, bt, kc[layer], vc[layer], out, 1 / math.sqrt(a), ws,
-                                          max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens)), window)
-            kd, vd = k.double().numpy(), v.double().numpy()
-            tok = 0
-            for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
-                for i in range(n):
-                    shadow[layer][(rid, c + i)] = (kd[tok], vd[tok])
-                    tok += 1
-            if check:
-                ks, vs = [], []
+        with torch.cuda.stream(stream):
+            m = sched.step()
+            steps += 1
+            preempted += m["n_preempted"]
+            b = len(m["req_ids"])
+            if b == 0:
+                continue
+            t = int(m["cu_q_lens"][-1])
+            cu = torch.from_numpy(m["cu_q_lens"]).cuda()
+            ctx = torch.from_numpy(m["ctx_lens"]).cuda()
+            bt = torch.from_numpy(np.ascontiguousarray(m["block_tables"])).cuda()
+            sl = torch.from_numpy(m["slot_mapping"]).cuda()
+            q_lens, ctx_lens = m["q_lens"].tolist(), m["ctx_lens"].tolist()
+            released += int((m["block_tables"] == -1).sum()) - sum(
+                max(0, maxblk - -(-(c + n) // bs)) for c, n in zip(ctx_lens, q_lens))
+            check = steps % 3 == 0 or m["n_preempted"] > 0
+            host = [(_bf16(rng, (t, hq, a)), _bf16(rng, (t, hk, a)), _bf16(rng, (t, hk, a))) for _ in range(nl)]
+            dev = [(q.cuda(), k.cuda(), v.cuda(), torch.empty(t, hq, a, dtype=torch.bfloat16, device="cuda"))
+                   for q, k, v in host]
+            kind = max(q_lens) > 1
+            rec = None
+            if graphs and kind in seen:
+                stream.synchronize()                   # the copies above are done before the recording starts
+                rec = recorders.setdefault(kind, lib.Graph())
+                rec.begin(stream)
+                recorded += 1
+            for layer in range(nl):
+                dq, dk, dv, out = dev[layer]
+                lib.cb_kv_append(dk, dv, sl, kc[layer], vc[layer])
+                lib.cb_paged_attention_window(dq, cu, ctx, bt, kc[layer], vc[layer], out, 1 / math.sqrt(a), ws,
+                                              max(q_lens), max(c + n for c, n in zip(ctx_lens, q_lens)), window)
+            if rec is not None:
+                rec.end(stream)
+            seen.add(kind)
+            for layer in range(nl):
+                q, k, v = host[layer]
+                out = dev[layer][3]
+                kd, vd = k.double().numpy(), v.double().numpy()
+                tok = 0
                 for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
-                    ks.append(np.stack([shadow[layer][(rid, p)][0] for p in range(c + n)]))
-                    vs.append(np.stack([shadow[layer][(rid, p)][1] for p in range(c + n)]))
-                ref = oa.attention_step(q.double().numpy(), q_lens, ctx_lens, ks, vs, 1 / math.sqrt(a), hq, hk,
-                                        window=window)
-                assert_close(out.double().cpu().numpy(), ref, f"step {steps} layer {layer}")
-                checked += 1
-        assert lib.cb_last_error() == 0
+                    for i in range(n):
+                        shadow[layer][(rid, c + i)] = (kd[tok], vd[tok])
+                        tok += 1
+                if check:
+                    ks, vs = [], []
+                    for rid, n, c in zip(m["req_ids"].tolist(), q_lens, ctx_lens):
+                        ks.append(np.stack([shadow[layer][(rid, p)][0] for p in range(c + n)]))
+                        vs.append(np.stack([shadow[layer][(rid, p)][1] for p in range(c + n)]))
+                    ref = oa.attention_step(q.double().numpy(), q_lens, ctx_lens, ks, vs, 1 / math.sqrt(a), hq, hk,
+                                            window=window)
+                    assert_close(out.double().cpu().numpy(), ref, f"step {steps} layer {layer}")
+                    checked += 1
+            assert lib.cb_last_error() == 0
     assert sched.done()
     assert checked > 20
+    if graphs:
+        assert recorded > 20, "most steps are meant to run as graphs"
     if num_blocks == 16:
         assert preempted > 0, "the tight pool is meant to exercise preemption"
     if window:
