@@ -37,11 +37,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
     tc_fence_before();
   }
-  append_phase(P, Ap);             // the step's new rows, when this launch stores them
+  append_phase<HKV == 8>(P, Ap);             // the step's new rows, when this launch stores them
   for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) bpre[r] = decode_blocks(P, r, false);
   __syncthreads();
   finish_plan<G, HKV>(P, C, bpre, slot);
-  append_wait(P, Ap);
+  if (threadIdx.x == 0) C.per_request = per_request_merge<G, HKV>(P, false);
+  append_wait<HKV == 8>(P, Ap);             // (its barrier publishes per_request too)
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   run_pipeline<G, HKV>(P, &kmap, &vmap, &qmap, T, C, bpre, slot, tmem, true);
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg<G, HKV>::TM);
   }
-  merge_phase<G, HKV>(P, C, slot, reinterpret_cast<float*>(&T.k[0][0][0][0]));   // the K ring is free now
+  merge_phase<G, HKV>(P, C, slot, reinterpret_cast<float*>(&T.k[0][0][0][0]), false);   // the K ring is free now
   release_counters(P);
 }
 

@@ -134,6 +134,8 @@ struct alignas(16) Ctl {
   uint32_t tmem_base;
   volatile int abort;
   int scratch[96];
+  int merge_ready;             // the current merge task's splits are all written (CTA-wide tasks)
+  int per_request;             // splits are counted per request and each merge waits for its own (no grid barrier)
 };
 
 // Single-thread bounded wait: on time-out records the error and raises abort.
@@ -1130,11 +1132,26 @@ __device__ void b_epilogue(const StepParams& P, Ctl<G, HKV>& C, uint32_t tmem) {
         P.part_ml[(base + tid) * 2] = C.ep[e].mmax[tid];
         P.part_ml[(base + tid) * 2 + 1] = C.ep[e].lsum[tid];
       }
+      if constexpr (HKV == 8)
+        if (C.per_request) __threadfence();   // this thread's share of the partial before the request's count
     }
     named_bar(2, 128);             // every thread is done with ep[e]
+    if constexpr (HKV == 8)
+      if (C.per_request && I.nsplit > 1 && tid == 0) atomicAdd(P.counters + I.r, 1);   // one more split written
     mbar_arrive(&C.ep_empty[e]);
     ++k;
   }
+}
+
+// Whether a launch merges each request as soon as its own splits are written
+// instead of after a grid-wide barrier: with 8 KV heads, unless other partial
+// results need the barrier (grid_sync).  With 1 or 2 KV heads the barrier
+// stays (the waits' code alone cost the MQA kernel registers and 7 %).  The
+// same in every CTA.
+template <int G, int HKV>
+__device__ __forceinline__ bool per_request_merge(const StepParams& P, bool grid_sync) {
+  (void)P;
+  return HKV == 8 && !grid_sync;   // compiled in only there: its registers cost the 1- and 2-head kernels
 }
 
 // ---------------------------------------------------------------- split merge (all warps of the grid)
@@ -1161,17 +1178,31 @@ static __device__ __noinline__ void append_store(const AppendParams& Ap, int64_t
   fence_proxy_async_global();
   __threadfence();
 }
+// With COUNT (launches whose merge may wait per request) it also zeroes its
+// share of the per-request split counters P.counters[0, n_reqs) before its
+// CTA arrives, and the launch meets at the counter even with no rows to store,
+// so the counters are zero wherever the pipeline counts.
+template <bool COUNT>
 __device__ __forceinline__ void append_phase(const StepParams& P, const AppendParams& Ap) {
-  if (Ap.n_tokens == 0) return;
-  append_store(Ap, (int64_t)P.num_blocks * kBlockSize, P.n_kv_heads, P.err);
+  if constexpr (COUNT) {
+    const int g0 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g0 < P.n_reqs) {
+      for (int r = g0; r < P.n_reqs; r += gridDim.x * blockDim.x) P.counters[r] = 0;
+      __threadfence();
+    }
+  } else if (Ap.n_tokens == 0) {
+    return;
+  }
+  if (Ap.n_tokens != 0) append_store(Ap, (int64_t)P.num_blocks * kBlockSize, P.n_kv_heads, P.err);
   __syncthreads();
   if (threadIdx.x == 0) atomicAdd(P.queue + 2, 1);
 }
 // Bounded wait until every CTA has arrived after its append stores; a time-out
 // records CB_DEVERR_TIMEOUT and goes on (the step's result is then unreliable,
 // and the host is told).  All threads of the CTA call it.
+template <bool COUNT>
 __device__ __forceinline__ void append_wait(const StepParams& P, const AppendParams& Ap) {
-  if (Ap.n_tokens == 0) return;
+  if (!COUNT && Ap.n_tokens == 0) return;
   if (threadIdx.x == 0) {
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu(P.queue + 2) < gridDim.x) {
@@ -1214,13 +1245,20 @@ __device__ __forceinline__ void release_counters(const StepParams& P) {
 // the CTA call it; red: nw * 128 floats of shared memory that nothing else
 // uses any more (the tile rings).
 template <int G, int HKV>
-__device__ void merge_phase(const StepParams& P, Ctl<G, HKV>& C, const int* slot, float* red) {
+__device__ void merge_phase(const StepParams& P, Ctl<G, HKV>& C, const int* slot, float* red, bool grid_sync) {
   constexpr int Hq = Cfg<G, HKV>::Hq;
   const unsigned FULL = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!C.split_any) return;        // every output was written by its only split
+  const int nw = blockDim.x >> 5;
+  const int n_task = P.n_reqs * Hq;
+  bool per_request = false;
+  if constexpr (HKV == 8) per_request = C.per_request;   // per_request_merge(P, grid_sync), set with the plan
+  (void)grid_sync;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (per_request) {
+    if (threadIdx.x == 0) C.merge_ok = 1;
+  } else if (threadIdx.x == 0) {
     C.merge_ok = 1;
     __threadfence();               // this CTA's partials before its arrival
     if (atomicAdd(P.queue + 1, 1) + 1 < gridDim.x) {
@@ -1239,8 +1277,6 @@ __device__ void merge_phase(const StepParams& P, Ctl<G, HKV>& C, const int* slot
   }
   __syncthreads();
   if (!C.merge_ok) return;
-  const int nw = blockDim.x >> 5;
-  const int n_task = P.n_reqs * Hq;
   // Few tasks: a CTA per (request, head), its warps sharing the splits and
   // adding their sums in shared memory (red: nw * 128 floats); else a warp per task.
   const bool cta_mode = n_task <= (int)gridDim.x;
@@ -1251,6 +1287,33 @@ __device__ void merge_phase(const StepParams& P, Ctl<G, HKV>& C, const int* slot
     const int i = task / Hq, h = task - i * Hq;
     const int slot0 = slot[i], ns = slot[i + 1] - slot0;
     if (ns <= 1) continue;         // the same for every warp of the task
+    if (HKV == 8 && per_request) {
+      // without the grid-wide barrier: wait (bounded) until every split of
+      // request i has written its partial, so a request's merge overlaps the
+      // other requests' streams
+      int ready = 1;
+      if (cta_mode ? threadIdx.x == 0 : lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while ((int)ld_acquire_gpu(P.counters + i) < ns) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs || C.abort) {
+            set_error(P.err, CB_DEVERR_TIMEOUT);
+            ready = 0;
+            break;
+          }
+          __nanosleep(32);
+        }
+        if (cta_mode) C.merge_ready = ready;
+      }
+      if (cta_mode) {
+        __syncthreads();
+        ready = C.merge_ready;
+        __syncthreads();           // merge_ready is read by every thread before the next task sets it
+      } else {
+        ready = __shfl_sync(FULL, ready, 0);
+      }
+      if (!ready) continue;
+      (void)ld_acquire_gpu(P.counters + i);   // this thread's reads of the partials come after the count
+    }
     // (m, l) of splits lane + 32k, k < 4, stay in registers; splits past 128 are re-read
     const float2* ml = reinterpret_cast<const float2*>(P.part_ml) + (size_t)slot0 * Hq + h;
     float2 v[4];

@@ -899,7 +899,7 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
   if constexpr (BT) {
     // prefill items per request and decode blocks per request, both in request order
     tcb::Ctl<G, HKV>& C2 = *reinterpret_cast<tcb::Ctl<G, HKV>*>(base + L::kRegion + sizeof(MixedCtl));
-    tcb::append_phase(P, Ap);      // the step's new rows, when this launch stores them
+    tcb::append_phase<HKV == 8>(P, Ap);      // the step's new rows, when this launch stores them
     for (int r = threadIdx.x; r < P.n_reqs; r += blockDim.x) {
       pre[r] = request_work(P, r, 2 * TOK, true).pre_items;
       a1[r] = tcb::decode_blocks(P, r, true);
@@ -910,7 +910,8 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
     prefill_plan<2 * TOK>(P, Sp, C, pre, (long long)C2.total * (2 * HKV * kBlockSize * A * 2),
                           reinterpret_cast<int*>(&T.q[0][0][0][0]));   // the tiles are free until the prefill
     if (threadIdx.x == 0 && C.pc_balanced) C2.split_any = 1;   // the pieces' merge needs the grid-wide barrier
-    tcb::append_wait(P, Ap);       // before the first TMA load of the cache
+    if (threadIdx.x == 0) C2.per_request = tcb::per_request_merge<G, HKV>(P, C.pc_balanced != 0);
+    tcb::append_wait<HKV == 8>(P, Ap);       // before the first TMA load of the cache
   } else {
     build_plan(P, 2 * TOK, a0, a1, a2, C.scratch);   // ends with __syncthreads()
   }
@@ -944,7 +945,9 @@ __global__ void __launch_bounds__(BT ? tcb::kThreads : kNumThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
-    tcb::merge_phase<G, HKV>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]));   // the K ring is free now
+    // the balanced prefill's pieces are merged after a grid-wide barrier; without
+    // them each request's merge waits only for its own splits
+    tcb::merge_phase<G, HKV>(P, C2, a2, reinterpret_cast<float*>(&T2.k[0][0][0][0]), C.pc_balanced != 0);
     if (C.pc_balanced && C2.merge_ok) prefill_merge<A, G>(P, Sp, C, pre);
     tcb::release_counters(P);
   } else {
